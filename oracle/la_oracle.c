@@ -1,0 +1,211 @@
+/*
+ * la_oracle.c -- fp64 CPU oracle for Bailing-style segmented lightning attention (seg_la).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this file: only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg do.  It shares no code, header or
+ * table with the CUDA library; both sides see only the same seeded inputs.
+ *
+ * Source of the method.  Page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析"
+ * (SGLang Lightning Attention capability matrix and seg_la test-coverage analysis), cited below as
+ * [LA-page].  Sections used:
+ *   [LA-page §独立参考实现]  "Independent reference implementation: per-token recurrence formula":
+ *       per head h:  state_t = state_{t-1} * exp(-slope_h) + outer(k_t, v_t)
+ *                    o_t     = q_t @ state_t * head_dim ** -0.5
+ *       looped token by token per request, final state written back at the end; prefix requests
+ *       start from a state injected into the state pool; the slope rule
+ *       slopes * (1 - layer_id/(L-1) + 1e-5), and slopes * (1 + 1e-5) when L = 1.
+ *   [LA-page §生产环境不支持 item 3]  chain (topk = 1) target verify: every draft token continues
+ *       from the previous position's state.
+ *
+ * Everything is evaluated in double precision straight from those definitions: no chunking, no
+ * blocking, no reassociation.  The state is S[i][j] with i on the k index (rows) and j on the v
+ * index (columns), so outer(k, v)[i][j] = k_i * v_j and (q @ S)[j] = sum_i q_i * S[i][j].
+ *
+ * Readings of points the page leaves open (each also listed in the design notes):
+ *   - base slopes are the ALiBi geometric sequence 2^(-8 (i+1) / H), i = 0..H-1;
+ *   - decay is applied before the outer product is added, so the current token has weight 1;
+ *   - a request whose prefix flag is 0 starts from the zero state and never reads its slot;
+ *   - the final state is written back for every request, including zero-length ones;
+ *   - chain verify leaves the pool untouched and records the state after each draft token.
+ *
+ * Threads: the (request, head) pairs are independent, so they are spread over POSIX threads.
+ * This changes no arithmetic: every pair is still one plain sequential loop.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* [LA-page §独立参考实现], the slope bullet: ALiBi-style per-head slope times the per-layer factor. */
+void la_oracle_slopes(int H, int layer_id, int L, double *out)
+{
+    double factor;
+    if (L == 1)
+        factor = 1.0 + 1e-5;
+    else
+        factor = 1.0 - (double)layer_id / (double)(L - 1) + 1e-5;
+    for (int i = 0; i < H; i++)
+        out[i] = pow(2.0, -8.0 * (double)(i + 1) / (double)H) * factor;
+}
+
+/* One request-head recurrence over n tokens, starting from S (in place).
+ * q, k, v point at the first token's head slice; row_stride is the distance between tokens.
+ * If inter != NULL, the state after token t is copied to inter + t * inter_stride. */
+static void recur(double *S, int D, double slope, int n, const double *q, const double *k,
+                  const double *v, size_t row_stride, double *out, double *inter,
+                  size_t inter_stride)
+{
+    const double decay = exp(-slope);
+    const double scale = 1.0 / sqrt((double)D);
+    for (int t = 0; t < n; t++) {
+        const double *qt = q + (size_t)t * row_stride;
+        const double *kt = k + (size_t)t * row_stride;
+        const double *vt = v + (size_t)t * row_stride;
+        /* state_t = state_{t-1} * exp(-slope) + outer(k_t, v_t) */
+        for (int i = 0; i < D; i++)
+            for (int j = 0; j < D; j++)
+                S[(size_t)i * D + j] = S[(size_t)i * D + j] * decay + kt[i] * vt[j];
+        /* o_t = q_t @ state_t * head_dim^-0.5 */
+        double *ot = out + (size_t)t * row_stride;
+        for (int j = 0; j < D; j++) {
+            double acc = 0.0;
+            for (int i = 0; i < D; i++)
+                acc += qt[i] * S[(size_t)i * D + j];
+            ot[j] = acc * scale;
+        }
+        if (inter)
+            memcpy(inter + (size_t)t * inter_stride, S, sizeof(double) * (size_t)D * D);
+    }
+}
+
+enum { OP_EXTEND = 0, OP_DECODE = 1, OP_VERIFY = 2 };
+
+typedef struct {
+    int op;
+    const double *q, *k, *v, *slopes;
+    double *pool;                 /* [num_slots][H][D][D] */
+    const int32_t *state_idx;     /* [B] */
+    const int32_t *cu_seqlens;    /* [B+1] (extend) */
+    const uint8_t *prefix_mask;   /* [B]   (extend) */
+    double *out;                  /* [T][H*D] */
+    double *inter;                /* [B][N][H][D][D] (verify) */
+    int B, H, D, N;
+    int nthreads;
+    int tid;
+} job_t;
+
+static void run_pair(const job_t *a, int b, int h)
+{
+    const int D = a->D, H = a->H;
+    const size_t row = (size_t)H * D, dd = (size_t)D * D;
+    double *slot = a->pool + ((size_t)a->state_idx[b] * H + h) * dd;
+    double *S = (double *)malloc(sizeof(double) * dd);
+    if (a->op == OP_EXTEND) {
+        /* [LA-page §独立参考实现], prefix-state injection: prefix requests start from the pool. */
+        if (a->prefix_mask[b])
+            memcpy(S, slot, sizeof(double) * dd);
+        else
+            memset(S, 0, sizeof(double) * dd);
+        const int t0 = a->cu_seqlens[b], n = a->cu_seqlens[b + 1] - t0;
+        const size_t off = (size_t)t0 * row + (size_t)h * D;
+        recur(S, D, a->slopes[h], n, a->q + off, a->k + off, a->v + off, row, a->out + off,
+              NULL, 0);
+        memcpy(slot, S, sizeof(double) * dd); /* final state written back at the end */
+    } else if (a->op == OP_DECODE) {
+        memcpy(S, slot, sizeof(double) * dd);
+        const size_t off = (size_t)b * row + (size_t)h * D;
+        recur(S, D, a->slopes[h], 1, a->q + off, a->k + off, a->v + off, row, a->out + off,
+              NULL, 0);
+        memcpy(slot, S, sizeof(double) * dd);
+    } else {
+        /* chain verify: token t of request b continues from token t-1; pool is only read */
+        memcpy(S, slot, sizeof(double) * dd);
+        const size_t off = (size_t)b * a->N * row + (size_t)h * D;
+        double *inter = a->inter + ((size_t)b * a->N * H + h) * dd;
+        recur(S, D, a->slopes[h], a->N, a->q + off, a->k + off, a->v + off, row, a->out + off,
+              inter, (size_t)H * dd);
+    }
+    free(S);
+}
+
+static void *worker(void *p)
+{
+    const job_t *a = (const job_t *)p;
+    const int pairs = a->B * a->H;
+    for (int w = a->tid; w < pairs; w += a->nthreads)
+        run_pair(a, w / a->H, w % a->H);
+    return NULL;
+}
+
+static int run(job_t *a)
+{
+    int nt = a->nthreads < 1 ? 1 : a->nthreads;
+    if (nt > a->B * a->H)
+        nt = a->B * a->H > 0 ? a->B * a->H : 1;
+    if (nt == 1) {
+        a->nthreads = 1;
+        a->tid = 0;
+        worker(a);
+        return 0;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nt);
+    job_t *jobs = (job_t *)malloc(sizeof(job_t) * nt);
+    for (int i = 0; i < nt; i++) {
+        jobs[i] = *a;
+        jobs[i].nthreads = nt;
+        jobs[i].tid = i;
+        if (pthread_create(&th[i], NULL, worker, &jobs[i]) != 0) {
+            /* fall back to running this share on the calling thread */
+            worker(&jobs[i]);
+            th[i] = 0;
+        }
+    }
+    for (int i = 0; i < nt; i++)
+        if (th[i])
+            pthread_join(th[i], NULL);
+    free(th);
+    free(jobs);
+    return 0;
+}
+
+/* Packed varlen extend: q, k, v, out are [T][H*D]; request b covers rows
+ * [cu_seqlens[b], cu_seqlens[b+1]); its state lives in pool[state_idx[b]]. */
+int la_oracle_extend(const double *q, const double *k, const double *v, const double *slopes,
+                     double *pool, const int32_t *state_idx, const int32_t *cu_seqlens,
+                     const uint8_t *prefix_mask, double *out, int B, int H, int D, int nthreads)
+{
+    job_t a = {0};
+    a.op = OP_EXTEND;
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool;
+    a.state_idx = state_idx; a.cu_seqlens = cu_seqlens; a.prefix_mask = prefix_mask;
+    a.out = out; a.B = B; a.H = H; a.D = D; a.N = 0; a.nthreads = nthreads;
+    return run(&a);
+}
+
+/* One-token decode: q, k, v, out are [B][H*D]; every request starts from its pool slot and the
+ * slot is updated in place. */
+int la_oracle_decode(const double *q, const double *k, const double *v, const double *slopes,
+                     double *pool, const int32_t *state_idx, double *out, int B, int H, int D,
+                     int nthreads)
+{
+    job_t a = {0};
+    a.op = OP_DECODE;
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool; a.state_idx = state_idx;
+    a.out = out; a.B = B; a.H = H; a.D = D; a.nthreads = nthreads;
+    return run(&a);
+}
+
+/* Chain verify: q, k, v, out are [B*N][H*D] (request-major, N draft tokens each); the pool is
+ * read only; inter is [B][N][H][D][D], the state after each draft token. */
+int la_oracle_verify_chain(const double *q, const double *k, const double *v,
+                           const double *slopes, const double *pool, const int32_t *state_idx,
+                           double *inter, double *out, int B, int N, int H, int D, int nthreads)
+{
+    job_t a = {0};
+    a.op = OP_VERIFY;
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = (double *)pool;
+    a.state_idx = state_idx; a.inter = inter; a.out = out;
+    a.B = B; a.H = H; a.D = D; a.N = N; a.nthreads = nthreads;
+    return run(&a);
+}

@@ -1,0 +1,97 @@
+"""Mutation check of the oracle pins.
+
+Each case below plants one plausible slip in a private copy of oracle/la_oracle.c (compiled with
+gcc into a temporary directory, on the CPU), binds it in place of the real oracle, and runs the
+pins of test_oracle_pins.py against it.  A slip that no pin catches fails this test.  The real
+oracle source is never modified.
+"""
+import inspect
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "la_oracle.c")
+
+MUTANTS = {
+    "decay_after_add": ("S[(size_t)i * D + j] = S[(size_t)i * D + j] * decay + kt[i] * vt[j];",
+                        "S[(size_t)i * D + j] = (S[(size_t)i * D + j] + kt[i] * vt[j]) * decay;"),
+    "decay_sign": ("const double decay = exp(-slope);", "const double decay = exp(slope);"),
+    "decay_dropped": ("S[(size_t)i * D + j] * decay + kt[i] * vt[j];",
+                      "S[(size_t)i * D + j] + kt[i] * vt[j];"),
+    "outer_transposed": ("* decay + kt[i] * vt[j];", "* decay + kt[j] * vt[i];"),
+    "scale_dropped": ("ot[j] = acc * scale;", "ot[j] = acc;"),
+    "scale_inverted": ("const double scale = 1.0 / sqrt((double)D);",
+                       "const double scale = sqrt((double)D);"),
+    "readout_transposed": ("acc += qt[i] * S[(size_t)i * D + j];",
+                           "acc += qt[i] * S[(size_t)j * D + i];"),
+    "prefix_ignored": ("if (a->prefix_mask[b])", "if (0)"),
+    "prefix_always_read": ("if (a->prefix_mask[b])", "if (1)"),
+    "final_state_not_written": ("memcpy(slot, S, sizeof(double) * dd); /* final state",
+                                "(void)slot; /* final state"),
+    "layer_factor_sign": ("factor = 1.0 - (double)layer_id / (double)(L - 1) + 1e-5;",
+                          "factor = 1.0 + (double)layer_id / (double)(L - 1) + 1e-5;"),
+    "layer_factor_eps_dropped": ("factor = 1.0 - (double)layer_id / (double)(L - 1) + 1e-5;",
+                                 "factor = 1.0 - (double)layer_id / (double)(L - 1);"),
+    "single_layer_factor": ("factor = 1.0 + 1e-5;", "factor = 1.0;"),
+    "alibi_index": ("pow(2.0, -8.0 * (double)(i + 1) / (double)H)",
+                    "pow(2.0, -8.0 * (double)i / (double)H)"),
+    "verify_writes_pool": ("inter, (size_t)H * dd);",
+                           "inter, (size_t)H * dd);\n        memcpy(slot, S, sizeof(double) * dd);"),
+    "verify_inter_lag": ("memcpy(inter + (size_t)t * inter_stride, S,",
+                         "memcpy(inter + (size_t)(t + 1 < n ? t + 1 : t) * inter_stride, S,"),
+    "decode_zero_start": ("        memcpy(S, slot, sizeof(double) * dd);\n"
+                          "        const size_t off = (size_t)b * row + (size_t)h * D;",
+                          "        memset(S, 0, sizeof(double) * dd);\n"
+                          "        const size_t off = (size_t)b * row + (size_t)h * D;"),
+    "request_length_short": ("n = a->cu_seqlens[b + 1] - t0;", "n = a->cu_seqlens[b + 1] - t0 - 1;"),
+    "wrong_head_slope": ("recur(S, D, a->slopes[h], n,", "recur(S, D, a->slopes[0], n,"),
+}
+
+
+def _pin_calls():
+    calls = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        params = inspect.signature(fn).parameters
+        if "split" in params:
+            for sp in (0, 64, 129):
+                calls.append((f"{name}[{sp}]", lambda fn=fn, sp=sp: fn(sp)))
+        elif not params:
+            calls.append((name, fn))
+    return calls
+
+
+@pytest.fixture(scope="module")
+def base_source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_mutant(mutant, base_source, tmp_path, monkeypatch):
+    old, new = MUTANTS[mutant]
+    assert base_source.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    src = base_source.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    so_path = tmp_path / "libmutant.so"
+    c_path.write_text(src)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so_path),
+                    str(c_path), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(so_path)))
+    caught = []
+    for name, call in _pin_calls():
+        try:
+            call()
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(name)
+    assert caught, f"no pin catches the planted slip '{mutant}'"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    for name, call in _pin_calls():
+        call()

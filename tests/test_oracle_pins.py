@@ -1,0 +1,239 @@
+"""Pins for the fp64 oracle: checks against what mathematics fixes, not against the oracle itself.
+
+The method (page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
+"独立参考实现：逐 token 递推公式") is the recurrence
+    S_t = S_{t-1} * exp(-s) + outer(k_t, v_t),    o_t = (q_t @ S_t) * D^-0.5.
+Unrolled, it has the closed form
+    o_t = D^-0.5 * [ e^{-s(t-t0+1)} q_t S_0 + sum_{u=t0..t} e^{-s(t-u)} (q_t . k_u) v_u ]
+    S_end = e^{-s n} S_0 + sum_u e^{-s(t1-1-u)} outer(k_u, v_u),
+which the tests below evaluate with independent O(T^2) loops.  Each pin is chosen so that a
+plausible slip in the oracle (dropped decay, decay applied after the add, transposed outer
+product, missing scale, wrong slot, wrong initial state) fails at least one of them; the mutation
+tests in test_oracle_mutants.py show that they do.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def rng_inputs(seed, T, H, D):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((T, H * D))
+    k = r.standard_normal((T, H * D))
+    v = r.standard_normal((T, H * D))
+    return q, k, v
+
+
+def closed_form(q, k, v, s, S0, D):
+    """O(T^2) closed form of the recurrence for one request-head (rows are tokens)."""
+    n = q.shape[0]
+    scale = 1.0 / math.sqrt(D)
+    out = np.zeros((n, D))
+    for t in range(n):
+        acc = math.exp(-s * (t + 1)) * (q[t] @ S0)
+        for u in range(t + 1):
+            acc = acc + math.exp(-s * (t - u)) * float(q[t] @ k[u]) * v[u]
+        out[t] = scale * acc
+    S = math.exp(-s * n) * S0
+    for u in range(n):
+        S = S + math.exp(-s * (n - 1 - u)) * np.outer(k[u], v[u])
+    return out, S
+
+
+def test_closed_form_varlen_with_prefix():
+    H, D = 2, 16
+    lens = [5, 0, 9, 1]
+    B = len(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v = rng_inputs(1, T, H, D)
+    slopes = np.array([0.3, 0.05])
+    r = np.random.default_rng(7)
+    num_slots = 6
+    pool = r.standard_normal((num_slots, H, D, D)) * 0.05
+    idx = np.array([4, 1, 0, 3], dtype=np.int32)
+    pm = np.array([1, 1, 0, 1], dtype=np.uint8)
+    out, pool_after = oracle.extend(q, k, v, slopes, pool, idx, cu, pm, H, D)
+    for b in range(B):
+        t0, t1 = cu[b], cu[b + 1]
+        for h in range(H):
+            sl = slice(h * D, (h + 1) * D)
+            S0 = pool[idx[b], h] if pm[b] else np.zeros((D, D))
+            o_ref, S_ref = closed_form(q[t0:t1, sl], k[t0:t1, sl], v[t0:t1, sl], slopes[h], S0, D)
+            np.testing.assert_allclose(out[t0:t1, sl], o_ref, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(pool_after[idx[b], h], S_ref, rtol=1e-12, atol=1e-13)
+    # the slot no request names is untouched, bit for bit
+    np.testing.assert_array_equal(pool_after[2], pool[2])
+    np.testing.assert_array_equal(pool_after[5], pool[5])
+
+
+def test_closed_form_head_dim_128():
+    H, D, n = 1, 128, 12
+    q, k, v = rng_inputs(3, n, H, D)
+    s = 0.7071
+    S0 = np.random.default_rng(4).standard_normal((D, D)) * 0.05
+    pool = S0[None, None].copy()
+    out, pool_after = oracle.extend(q, k, v, [s], pool, [0], [0, n], [1], H, D)
+    o_ref, S_ref = closed_form(q, k, v, s, S0, D)
+    np.testing.assert_allclose(out, o_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(pool_after[0, 0], S_ref, rtol=1e-11, atol=1e-12)
+
+
+def test_geometric_series_scalar_head():
+    """D = 1, q = k = v = 1, slope ln 2: S_t = c 2^-t + 2 - 2^(1-t) and o_t = S_t (scale 1)."""
+    n, c = 10, 0.75
+    ones = np.ones((n, 1))
+    out, pool_after = oracle.extend(ones, ones, ones, [math.log(2.0)], np.full((1, 1, 1, 1), c),
+                                    [0], [0, n], [1], 1, 1)
+    t = np.arange(1, n + 1, dtype=np.float64)
+    expect = c * 2.0 ** -t + 2.0 - 2.0 ** (1 - t)
+    np.testing.assert_allclose(out[:, 0], expect, rtol=1e-14)
+    assert abs(pool_after[0, 0, 0, 0] - expect[-1]) < 1e-14
+
+
+def test_zero_slope_is_prefix_sum():
+    """s = 0: o_t = D^-0.5 q_t (S_0 + sum_{u<=t} k_u v_u^T), a cumulative sum of outer products."""
+    H, D, n = 1, 8, 20
+    q, k, v = rng_inputs(5, n, H, D)
+    S0 = np.random.default_rng(6).standard_normal((D, D))
+    out, pool_after = oracle.extend(q, k, v, [0.0], S0[None, None], [0], [0, n], [1], H, D)
+    outer = np.einsum("ti,tj->tij", k, v)
+    S = S0[None] + np.cumsum(outer, axis=0)
+    ref = np.einsum("ti,tij->tj", q, S) / math.sqrt(D)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(pool_after[0, 0], S[-1], rtol=1e-12, atol=1e-12)
+
+
+def test_large_slope_limit():
+    """s = 50: every older contribution is damped by e^-50, so o_t = D^-0.5 (q_t . k_t) v_t."""
+    H, D, n = 1, 8, 6
+    q, k, v = rng_inputs(8, n, H, D)
+    S0 = np.ones((1, 1, D, D))
+    out, _ = oracle.extend(q, k, v, [50.0], S0, [0], [0, n], [1], H, D)
+    ref = np.einsum("ti,ti->t", q, k)[:, None] * v / math.sqrt(D)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-18)
+
+
+@pytest.mark.parametrize("split", [0, 1, 7, 63, 64, 65, 127, 128, 129, 199, 200])
+def test_split_invariance(split):
+    """Extend of A then extend of B (prefix taken from the state A wrote) equals extend of A||B."""
+    H, D, n = 2, 8, 200
+    q, k, v = rng_inputs(9, n, H, D)
+    slopes = np.array([0.2, 0.01])
+    S0 = np.random.default_rng(10).standard_normal((3, H, D, D)) * 0.05
+    full_out, full_pool = oracle.extend(q, k, v, slopes, S0, [2], [0, n], [1], H, D)
+    o1, p1 = oracle.extend(q[:split], k[:split], v[:split], slopes, S0, [2], [0, split], [1], H, D)
+    o2, p2 = oracle.extend(q[split:], k[split:], v[split:], slopes, p1, [2], [0, n - split], [1],
+                           H, D)
+    np.testing.assert_allclose(np.concatenate([o1, o2]), full_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(p2, full_pool, rtol=1e-12, atol=1e-13)
+
+
+def test_decode_equals_length_one_extend():
+    H, D, B = 2, 16, 5
+    q, k, v = rng_inputs(11, B, H, D)
+    slopes = np.array([0.5, 0.001])
+    pool = np.random.default_rng(12).standard_normal((8, H, D, D)) * 0.05
+    idx = np.array([6, 0, 3, 2, 7], dtype=np.int32)
+    d_out, d_pool = oracle.decode(q, k, v, slopes, pool, idx, H, D)
+    e_out, e_pool = oracle.extend(q, k, v, slopes, pool, idx, np.arange(B + 1, dtype=np.int32),
+                                  np.ones(B, np.uint8), H, D)
+    np.testing.assert_array_equal(d_out, e_out)
+    np.testing.assert_array_equal(d_pool, e_pool)
+    # and against the one-step closed form: S' = e^-s S + k v^T, o = D^-0.5 q S'
+    for b in range(B):
+        for h in range(H):
+            sl = slice(h * D, (h + 1) * D)
+            S1 = math.exp(-slopes[h]) * pool[idx[b], h] + np.outer(k[b, sl], v[b, sl])
+            np.testing.assert_allclose(d_pool[idx[b], h], S1, rtol=1e-14, atol=1e-16)
+            np.testing.assert_allclose(d_out[b, sl], q[b, sl] @ S1 / math.sqrt(D), rtol=1e-12,
+                                       atol=1e-14)
+
+
+def test_verify_equals_extend_prefixes():
+    H, D, B, N = 2, 8, 3, 4
+    q, k, v = rng_inputs(13, B * N, H, D)
+    slopes = np.array([0.9, 0.02])
+    pool = np.random.default_rng(14).standard_normal((5, H, D, D)) * 0.05
+    pool_before = pool.copy()
+    idx = np.array([3, 0, 4], dtype=np.int32)
+    out, inter = oracle.verify_chain(q, k, v, slopes, pool, idx, N, H, D)
+    np.testing.assert_array_equal(pool, pool_before)  # the pool is only read
+    for b in range(B):
+        rows = slice(b * N, (b + 1) * N)
+        e_out, _ = oracle.extend(q[rows], k[rows], v[rows], slopes, pool, [idx[b]], [0, N], [1],
+                                 H, D)
+        np.testing.assert_allclose(out[rows], e_out, rtol=1e-13, atol=1e-15)
+        for t in range(N):
+            _, p = oracle.extend(q[rows][: t + 1], k[rows][: t + 1], v[rows][: t + 1], slopes,
+                                 pool, [idx[b]], [0, t + 1], [1], H, D)
+            np.testing.assert_allclose(inter[b, t], p[idx[b]], rtol=1e-13, atol=1e-15)
+
+
+def test_linearity():
+    H, D, n = 1, 8, 15
+    q, k, v = rng_inputs(15, n, H, D)
+    _, _, v2 = rng_inputs(16, n, H, D)
+    z = np.zeros((1, 1, D, D))
+    s = [0.1]
+    o1, _ = oracle.extend(q, k, v, s, z, [0], [0, n], [0], H, D)
+    o2, _ = oracle.extend(q, k, v2, s, z, [0], [0, n], [0], H, D)
+    o12, _ = oracle.extend(q, k, 2.0 * v + 3.0 * v2, s, z, [0], [0, n], [0], H, D)
+    np.testing.assert_allclose(o12, 2.0 * o1 + 3.0 * o2, rtol=1e-12, atol=1e-12)
+    oq, _ = oracle.extend(-0.5 * q, k, v, s, z, [0], [0, n], [0], H, D)
+    np.testing.assert_allclose(oq, -0.5 * o1, rtol=1e-13, atol=1e-14)
+    ok, pk = oracle.extend(q, 4.0 * k, v, s, z, [0], [0, n], [0], H, D)
+    np.testing.assert_allclose(ok, 4.0 * o1, rtol=1e-13, atol=1e-14)
+
+
+def test_prefix_flag_zero_never_reads_slot():
+    H, D, n = 1, 8, 9
+    q, k, v = rng_inputs(17, n, H, D)
+    nan_pool = np.full((2, H, D, D), np.nan)
+    out, pool_after = oracle.extend(q, k, v, [0.3], nan_pool, [1], [0, n], [0], H, D)
+    assert np.isfinite(out).all() and np.isfinite(pool_after[1]).all()
+    assert np.isnan(pool_after[0]).all()  # untouched slot keeps its contents
+    z_out, z_pool = oracle.extend(q, k, v, [0.3], np.zeros((2, H, D, D)), [1], [0, n], [1], H, D)
+    np.testing.assert_array_equal(out, z_out)
+    np.testing.assert_array_equal(pool_after[1], z_pool[1])
+
+
+def test_zero_length_request_writes_initial_state_back():
+    H, D = 1, 4
+    pool = np.random.default_rng(18).standard_normal((3, H, D, D))
+    q = np.zeros((0, H * D))
+    out, p = oracle.extend(q, q, q, [0.4], pool, [0, 2], [0, 0, 0], [1, 0], H, D)
+    assert out.shape == (0, H * D)
+    np.testing.assert_array_equal(p[0], pool[0])     # prefix kept as is
+    np.testing.assert_array_equal(p[2], np.zeros((H, D, D)))  # no prefix: zero state written
+    np.testing.assert_array_equal(p[1], pool[1])     # untouched
+
+
+def test_slope_rule():
+    """ALiBi base 2^(-8(i+1)/H) times (1 - l/(L-1) + 1e-5), or (1 + 1e-5) when L = 1."""
+    s = oracle.slopes(8, 0, 1)
+    base = np.array([2.0 ** -(i + 1) for i in range(8)])  # H = 8: 1/2, 1/4, ..., 1/256, exact
+    np.testing.assert_allclose(s, base * (1 + 1e-5), rtol=1e-15)
+    np.testing.assert_allclose(oracle.slopes(8, 0, 4), base * (1 + 1e-5), rtol=1e-15)
+    np.testing.assert_allclose(oracle.slopes(8, 3, 4), base * 1e-5, rtol=1e-10)
+    np.testing.assert_allclose(oracle.slopes(16, 3, 8), 2.0 ** (-0.5 * np.arange(1, 17))
+                               * (1 - 3 / 7 + 1e-5), rtol=1e-15)
+    # H = 2: 2^-4 and 2^-8
+    np.testing.assert_allclose(oracle.slopes(2, 0, 1), np.array([1 / 16, 1 / 256]) * (1 + 1e-5),
+                               rtol=1e-15)
+
+
+def test_thread_count_does_not_change_results():
+    H, D = 3, 8
+    lens = [4, 7, 1, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v = rng_inputs(19, int(cu[-1]), H, D)
+    pool = np.random.default_rng(20).standard_normal((4, H, D, D))
+    args = (q, k, v, [0.1, 0.2, 0.3], pool, [3, 1, 0, 2], cu, [1, 0, 1, 1], H, D)
+    o1, p1 = oracle.extend(*args, nthreads=1)
+    o8, p8 = oracle.extend(*args, nthreads=8)
+    np.testing.assert_array_equal(o1, o8)
+    np.testing.assert_array_equal(p1, p8)
