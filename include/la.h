@@ -1,0 +1,164 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) seg_la library: Bailing-style segmented lightning
+ * attention, i.e. per-head linear attention with an ALiBi-style exponential decay.
+ *
+ * Method source: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析"
+ * (SGLang Lightning Attention capability matrix and seg_la test-coverage analysis), cited as
+ * [LA-page].  Its section "独立参考实现：逐 token 递推公式" defines, per head h,
+ *     S_t = S_{t-1} * exp(-slope_h) + outer(k_t, v_t)          (S is head_dim x head_dim)
+ *     o_t = (q_t @ S_t) * head_dim^-0.5
+ * run over each request's tokens, starting from the request's state in a state pool and writing
+ * the final state back.
+ *
+ * Conventions shared by every call
+ *   - Element types: q, k, v and out are bfloat16 (passed as their 16-bit patterns, la_bf16);
+ *     states and slopes are IEEE fp32; indices are int32; flags are uint8.
+ *   - Token layout: a token's row is [H * D] with head h at columns [h*D, (h+1)*D), rows packed
+ *     back to back (row stride H*D elements).  This flat [T, H*D] layout is the one the page's
+ *     section "生产环境不支持" item 4 describes for the backend's extend and decode output.
+ *   - State layout: state_pool is [num_slots][H][D][D] fp32, row-major; in each D x D block the
+ *     row index runs over the k dimension and the column index over the v dimension, so
+ *     outer(k, v)[i][j] = k_i v_j and (q @ S)[j] = sum_i q_i S[i][j].
+ *   - Only head_dim D = 128 is supported (LA_ERR_UNSUPPORTED otherwise), in the spirit of the
+ *     head-dim entry guards the page's section "输入与配置覆盖" describes.  q, k and v share one
+ *     head count H (no grouped-query heads), as the same section states for seg_la.
+ *   - Pointers marked "device" must be device memory of the current CUDA device (or managed
+ *     memory); "host" pointers are host memory.  The caller owns every buffer; the library keeps
+ *     no pointer after a call returns and allocates no device memory.
+ *   - Every device call is asynchronous on `stream` (a cudaStream_t; NULL means the legacy
+ *     default stream) and does no host synchronisation, so it can be captured in a CUDA graph.
+ *     A status of LA_OK means the arguments passed the host checks and the launch succeeded.
+ *     Faults the host cannot see (a slot index out of range, inconsistent cu_seqlens, a device
+ *     wait that ran out) are recorded in a per-device error word and reported by la_poll_error.
+ *   - Preconditions the host cannot check: the state_idx entries of one call are distinct and lie
+ *     in [0, num_slots); cu_seqlens is non-decreasing, starts at 0 and ends at T; out overlaps no
+ *     input; inputs are finite.  Out-of-range slots and inconsistent cu_seqlens are detected on
+ *     the device (the affected request is skipped and the error word set); duplicate slots and
+ *     overlapping buffers give undefined results.
+ *   - Argument errors (NULL pointers with B > 0, negative sizes, H < 1, num_slots < 1 ...) return
+ *     LA_ERR_INVALID before anything is launched.  B = 0 is a no-op returning LA_OK.
+ */
+#ifndef LA_GB300_H
+#define LA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID = 1,      /* bad argument, detected on the host before any launch */
+    LA_ERR_UNSUPPORTED = 2,  /* valid but unsupported configuration (head_dim != 128, ...) */
+    LA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    LA_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (reported by la_poll_error) */
+    LA_ERR_DEVICE_INPUT = 5  /* the device found a slot index out of range or inconsistent
+                                cu_seqlens (reported by la_poll_error) */
+} la_status;
+
+typedef uint16_t la_bf16; /* bfloat16 bit pattern */
+typedef void *la_stream;  /* cudaStream_t */
+
+/*
+ * la_slopes -- per-head decay slopes for one layer (host only, no device work).
+ * [LA-page §独立参考实现], slope bullet: the ALiBi-style slopes times (1 - layer_id/(L-1) + 1e-5),
+ * or times (1 + 1e-5) when L = 1.  The ALiBi base is the geometric sequence 2^(-8 (i+1) / H),
+ * i = 0..H-1 (the page says only "ALiBi style"; this is that sequence for any H).
+ * Computed in double precision and rounded once to fp32.
+ *   H         number of heads, >= 1
+ *   layer_id  0 <= layer_id < L
+ *   L         number of layers, >= 1
+ *   host_out  host buffer of H floats, written on success
+ * Returns LA_ERR_INVALID for H < 1, L < 1, layer_id outside [0, L) or host_out == NULL.
+ */
+la_status la_slopes(int H, int layer_id, int L, float *host_out);
+
+/*
+ * la_extend -- packed varlen extend (prefill) over the state pool.
+ * [LA-page §独立参考实现]: for each request b and head h, start from
+ *     S = prefix_mask[b] ? state_pool[state_idx[b], h] : 0
+ * run the recurrence over the request's tokens, write o_t to out, and write the final S back to
+ * state_pool[state_idx[b], h] (also when prefix_mask[b] = 0, and for zero-length requests).
+ *   q, k, v      device, bf16 [T][H*D]; request b owns rows [cu_seqlens[b], cu_seqlens[b+1])
+ *   slopes       device, fp32 [H] (for example from la_slopes)
+ *   state_pool   device, fp32 [num_slots][H][D][D], read and updated in place; only the slots
+ *                named in state_idx are touched
+ *   num_slots    number of pool slots, >= 1
+ *   state_idx    device, int32 [B]
+ *   cu_seqlens   device, int32 [B+1]
+ *   prefix_mask  device, uint8 [B]; nonzero = start from the pool slot, 0 = start from zero
+ *                (the slot is then never read)
+ *   out          device, bf16 [T][H*D], written
+ *   B, T, H, D   requests, total tokens (= cu_seqlens[B]), heads, head_dim (must be 128)
+ *   max_seqlen   an upper bound on every request's length (T is always a valid value)
+ *   stream       cudaStream_t
+ * Numerics: bf16 inputs; fp32 states and accumulation; the intra-chunk products run on the
+ * tensor cores with bf16 operands and fp32 accumulators; out is rounded to bf16 once.
+ */
+la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                    float *state_pool, int num_slots, const int32_t *state_idx,
+                    const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
+                    int T, int H, int D, int max_seqlen, la_stream stream);
+
+/*
+ * la_decode -- one decode token per request, state updated in place.
+ * The recurrence of [LA-page §独立参考实现] for a single token; the page's section
+ * "输入与配置覆盖" names the matching decode kernel.  For each request b and head h:
+ *     S = state_pool[state_idx[b], h];  S = S * exp(-slopes[h]) + outer(k_b, v_b);
+ *     out_b = (q_b @ S) * D^-0.5;       state_pool[state_idx[b], h] = S
+ *   q, k, v     device, bf16 [B][H*D]
+ *   slopes      device, fp32 [H]
+ *   state_pool  device, fp32 [num_slots][H][D][D], updated in place (named slots only)
+ *   state_idx   device, int32 [B]
+ *   out         device, bf16 [B][H*D], written
+ */
+la_status la_decode(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                    float *state_pool, int num_slots, const int32_t *state_idx, la_bf16 *out,
+                    int B, int H, int D, la_stream stream);
+
+/*
+ * la_verify_chain -- chain (topk = 1) target verify of N draft tokens per request.
+ * [LA-page §生产环境不支持, item 3]: seg_la treats draft tokens as a chain, each one continuing
+ * from the previous position's state; tree verify is not supported (the page's backend refuses
+ * topk > 1), and neither is it here.  For each request b and head h, from
+ * S = state_pool[state_idx[b], h], for t = 0..N-1: apply the recurrence to token b*N + t, write
+ * its output row, and store S into inter_states[b][t][h].  The pool is only read; committing an
+ * accepted draft state is the caller's copy from inter_states.
+ *   q, k, v       device, bf16 [B*N][H*D] (request-major: request b owns rows b*N .. b*N+N-1)
+ *   slopes        device, fp32 [H]
+ *   state_pool    device, fp32 [num_slots][H][D][D], read only
+ *   state_idx     device, int32 [B]
+ *   inter_states  device, fp32 [B][N][H][D][D], written
+ *   out           device, bf16 [B*N][H*D], written
+ *   N             draft tokens per request, >= 1
+ */
+la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                          const float *slopes, const float *state_pool, int num_slots,
+                          const int32_t *state_idx, float *inter_states, la_bf16 *out, int B,
+                          int N, int H, int D, la_stream stream);
+
+/*
+ * la_poll_error -- synchronise `stream`, then read and clear the current device's error word.
+ * Returns LA_ERR_TIMEOUT if a bounded device wait ran out, LA_ERR_DEVICE_INPUT if a kernel found
+ * a slot index out of range or inconsistent cu_seqlens, LA_ERR_CUDA if the stream reports a CUDA
+ * error, else LA_OK.  This is the one call that blocks the host.
+ */
+la_status la_poll_error(la_stream stream);
+
+/* la_status_string -- static, human-readable name of a status code (never NULL). */
+const char *la_status_string(la_status status);
+
+/*
+ * la_set_wait_limit -- diagnostics: the number of polls after which a device wait in the extend
+ * kernel gives up, sets the error word and lets the kernel exit cleanly (0 restores the default,
+ * which is far above any legitimate wait).  Host only; affects later launches from this process.
+ * Lets a test drive the timeout path without hanging or faulting the GPU.
+ */
+void la_set_wait_limit(uint64_t polls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_GB300_H */

@@ -1,0 +1,8 @@
+"""seg_la on GB300: Bailing-style segmented lightning attention behind a C ABI.
+
+The computation runs in hand-written sm_103a CUDA kernels (csrc/), reached through the C ABI of
+include/la.h; this package holds the ctypes binding (binding.py), the in-tree build (_build.py)
+and the seeded synthetic workloads (workloads.py).
+"""
+from .binding import (LAError, decode, extend, load, poll_error, set_wait_limit, slopes,  # noqa
+                      verify_chain)

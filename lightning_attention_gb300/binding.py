@@ -1,0 +1,186 @@
+"""ctypes binding of the seg_la C ABI (include/la.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA library.  Tensors are
+checked for device, dtype, shape and contiguity, their ``data_ptr()`` and the current CUDA stream
+are passed through, and a non-OK status raises ``LAError``.  PyTorch provides device memory and
+streams; outputs the caller does not pass are allocated here with ``torch.empty``.
+
+If the compiled library is missing or cannot be loaded, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
+          4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
+
+EXPORTS = ("la_slopes", "la_extend", "la_decode", "la_verify_chain", "la_poll_error",
+           "la_status_string", "la_set_wait_limit")
+
+
+class LAError(RuntimeError):
+    def __init__(self, func: str, status: int, message: str):
+        super().__init__(f"{func} failed: {message}")
+        self.status = status
+        self.func = func
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the compiled library (building nothing); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"seg_la CUDA library not found at {path}; build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_float)
+        lib.la_slopes.argtypes = [ip, ip, ip, fp]
+        lib.la_slopes.restype = ip
+        lib.la_extend.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp]
+        lib.la_extend.restype = ip
+        lib.la_decode.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, vp]
+        lib.la_decode.restype = ip
+        lib.la_verify_chain.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, ip, ip, ip, ip, vp]
+        lib.la_verify_chain.restype = ip
+        lib.la_poll_error.argtypes = [vp]
+        lib.la_poll_error.restype = ip
+        lib.la_status_string.argtypes = [ip]
+        lib.la_status_string.restype = ctypes.c_char_p
+        lib.la_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.la_set_wait_limit.restype = None
+        _lib = lib
+        return lib
+
+
+def _check(func: str, status: int):
+    if status != 0:
+        msg = load().la_status_string(status).decode()
+        raise LAError(func, status, msg)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def slopes(H: int, layer_id: int, L: int) -> torch.Tensor:
+    """Per-head slopes (fp32, on the host) from the library's slope rule."""
+    out = (ctypes.c_float * H)() if H > 0 else (ctypes.c_float * 1)()
+    _check("la_slopes", load().la_slopes(H, layer_id, L, out))
+    return torch.tensor(list(out)[:H], dtype=torch.float32)
+
+
+def set_wait_limit(polls: int) -> None:
+    load().la_set_wait_limit(int(polls))
+
+
+def poll_error(device=None) -> None:
+    """Synchronise the current stream and raise if a kernel recorded a device-side fault."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check("la_poll_error", load().la_poll_error(_stream_handle(dev)))
+
+
+def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
+           max_seqlen: int | None = None):
+    """Packed varlen extend (la_extend).  q, k, v: bf16 [T, H*D]; state_pool fp32
+    [S, H, D, D] updated in place; returns out bf16 [T, H*D]."""
+    dev = q.device
+    T = q.shape[0]
+    num_slots, H, D, D2 = state_pool.shape
+    B = state_idx.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (T, H * D))
+    _need(slopes_, "slopes", torch.float32, dev, (H,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, (B + 1,))
+    _need(prefix_mask, "prefix_mask", torch.uint8, dev, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (T, H * D))
+    if max_seqlen is None:
+        max_seqlen = T
+    with torch.cuda.device(dev):
+        st = load().la_extend(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool), num_slots,
+                              _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask), _ptr(out), B, T,
+                              H, D, int(max_seqlen), _stream_handle(dev))
+    _check("la_extend", st)
+    return out
+
+
+def decode(q, k, v, slopes_, state_pool, state_idx, out=None):
+    """One-token decode (la_decode).  q, k, v: bf16 [B, H*D]; pool updated in place."""
+    dev = q.device
+    num_slots, H, D, _ = state_pool.shape
+    B = state_idx.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (B, H * D))
+    _need(slopes_, "slopes", torch.float32, dev, (H,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (B, H * D))
+    with torch.cuda.device(dev):
+        st = load().la_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool), num_slots,
+                              _ptr(state_idx), _ptr(out), B, H, D, _stream_handle(dev))
+    _check("la_decode", st)
+    return out
+
+
+def verify_chain(q, k, v, slopes_, state_pool, state_idx, N: int, inter_states=None, out=None):
+    """Chain verify (la_verify_chain).  q, k, v: bf16 [B*N, H*D]; returns (out, inter_states)
+    with inter_states fp32 [B, N, H, D, D]; the pool is not modified."""
+    dev = q.device
+    num_slots, H, D, _ = state_pool.shape
+    B = state_idx.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (B * N, H * D))
+    _need(slopes_, "slopes", torch.float32, dev, (H,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    if inter_states is None:
+        inter_states = torch.empty((B, N, H, D, D), dtype=torch.float32, device=dev)
+    _need(inter_states, "inter_states", torch.float32, dev, (B, N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (B * N, H * D))
+    with torch.cuda.device(dev):
+        st = load().la_verify_chain(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                    num_slots, _ptr(state_idx), _ptr(inter_states), _ptr(out), B,
+                                    N, H, D, _stream_handle(dev))
+    _check("la_verify_chain", st)
+    return out, inter_states

@@ -1,0 +1,182 @@
+// la_api.cu -- the extern "C" entry points of the seg_la library (declared in include/la.h):
+// host-side argument checks, the per-device error word, and kernel dispatch.  No entry point
+// allocates device memory or synchronises, except la_poll_error, which synchronises by design.
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "la.h"
+#include "la_internal.h"
+
+namespace {
+
+// Per-device error word: kernels OR bits into it when they find a fault the host cannot see
+// (out-of-range slot, inconsistent cu_seqlens, a bounded wait that ran out).  Module-scope
+// device variable; its address is looked up once per device and passed to kernels.
+__device__ unsigned int g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int *g_err_ptr[kMaxDevices] = {nullptr};
+std::atomic<unsigned long long> g_wait_limit{0};
+
+// Far above any legitimate wait (each poll is a try_wait with a hardware time hint), small enough
+// that a lost arrival ends the kernel in about a second instead of hanging the GPU.
+constexpr unsigned long long kDefaultWaitLimit = 1ull << 22;
+
+la_status error_word_ptr(unsigned int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return LA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return LA_OK;
+}
+
+la_status launch_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *la_status_string(la_status status) {
+    switch (status) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID: return "LA_ERR_INVALID: invalid argument";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: unsupported configuration";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch error";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device wait ran out";
+        case LA_ERR_DEVICE_INPUT:
+            return "LA_ERR_DEVICE_INPUT: slot index out of range or inconsistent cu_seqlens";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+la_status la_slopes(int H, int layer_id, int L, float *host_out) {
+    if (H < 1 || L < 1 || layer_id < 0 || layer_id >= L || host_out == nullptr)
+        return LA_ERR_INVALID;
+    // Per-layer factor from the page's slope rule; ALiBi geometric base 2^(-8 (i+1) / H).
+    const double factor =
+        (L == 1) ? (1.0 + 1e-5) : (1.0 - (double)layer_id / (double)(L - 1) + 1e-5);
+    for (int i = 0; i < H; ++i)
+        host_out[i] = (float)(exp2(-8.0 * (double)(i + 1) / (double)H) * factor);
+    return LA_OK;
+}
+
+void la_set_wait_limit(uint64_t polls) { g_wait_limit.store(polls); }
+
+la_status la_poll_error(la_stream stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    unsigned int *err = nullptr;
+    la_status st = error_word_ptr(&err);
+    if (st != LA_OK) return st;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return LA_ERR_CUDA;
+    }
+    if (word & la::ERR_BIT_TIMEOUT) return LA_ERR_TIMEOUT;
+    if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS)) return LA_ERR_DEVICE_INPUT;
+    return LA_OK;
+}
+
+la_status la_decode(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                    float *state_pool, int num_slots, const int32_t *state_idx, la_bf16 *out,
+                    int B, int H, int D, la_stream stream) {
+    if (B < 0 || H < 1 || D < 1 || num_slots < 1) return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (B == 0) return LA_OK;
+    if (!q || !k || !v || !slopes || !state_pool || !state_idx || !out) return LA_ERR_INVALID;
+    la::RecurParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.slopes = slopes;
+    p.pool = state_pool;
+    p.state_idx = state_idx;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.B = B;
+    p.H = H;
+    p.N = 1;
+    p.T = B;
+    p.num_slots = num_slots;
+    la_status st = error_word_ptr(&p.err);
+    if (st != LA_OK) return st;
+    return launch_status(la::launch_recurrent(la::RECUR_DECODE, p, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                          const float *slopes, const float *state_pool, int num_slots,
+                          const int32_t *state_idx, float *inter_states, la_bf16 *out, int B,
+                          int N, int H, int D, la_stream stream) {
+    if (B < 0 || N < 1 || H < 1 || D < 1 || num_slots < 1) return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * N > 0x7fffffffLL) return LA_ERR_INVALID;
+    if (B == 0) return LA_OK;
+    if (!q || !k || !v || !slopes || !state_pool || !state_idx || !inter_states || !out)
+        return LA_ERR_INVALID;
+    la::RecurParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.slopes = slopes;
+    p.pool = const_cast<float *>(state_pool);  // read only in verify mode
+    p.state_idx = state_idx;
+    p.inter = inter_states;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.T = B * N;
+    p.num_slots = num_slots;
+    la_status st = error_word_ptr(&p.err);
+    if (st != LA_OK) return st;
+    return launch_status(la::launch_recurrent(la::RECUR_VERIFY, p, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                    float *state_pool, int num_slots, const int32_t *state_idx,
+                    const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
+                    int T, int H, int D, int max_seqlen, la_stream stream) {
+    if (B < 0 || T < 0 || H < 1 || D < 1 || num_slots < 1 || max_seqlen < 0)
+        return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (B == 0) return LA_OK;
+    if (!slopes || !state_pool || !state_idx || !cu_seqlens || !prefix_mask) return LA_ERR_INVALID;
+    if (T > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID;
+    if ((long long)T * H * D >= (1ll << 40)) return LA_ERR_UNSUPPORTED;
+    la_status st;
+    unsigned int *err = nullptr;
+    if ((st = error_word_ptr(&err)) != LA_OK) return st;
+    la::RecurParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.slopes = slopes;
+    p.pool = state_pool;
+    p.state_idx = state_idx;
+    p.cu_seqlens = cu_seqlens;
+    p.prefix_mask = prefix_mask;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err;
+    p.B = B;
+    p.H = H;
+    p.T = T;
+    p.num_slots = num_slots;
+    return launch_status(la::launch_recurrent(la::RECUR_EXTEND, p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// la_internal.h -- declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+// Bits of the per-device error word (see la_api.cu).
+enum : unsigned int {
+    ERR_BIT_TIMEOUT = 1u,       // a bounded device wait ran out
+    ERR_BIT_SLOT_RANGE = 2u,    // state_idx entry outside [0, num_slots)
+    ERR_BIT_SEQLENS = 4u,       // cu_seqlens decreasing or past T
+};
+
+constexpr int kHeadDim = 128;
+
+// Recurrent (token-serial) kernels: decode, chain verify, and short extends.
+enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2 };
+
+struct RecurParams {
+    const __nv_bfloat16 *q, *k, *v;
+    const float *slopes;
+    float *pool;                 // [num_slots][H][D][D]
+    const int32_t *state_idx;    // [B]
+    const int32_t *cu_seqlens;   // [B+1] (extend)
+    const uint8_t *prefix_mask;  // [B]   (extend)
+    float *inter;                // [B][N][H][D][D] (verify)
+    __nv_bfloat16 *out;
+    unsigned int *err;           // device error word
+    int B, H, N, T, num_slots;
+};
+
+cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream);
+
+// Chunked tensor-core extend (tcgen05 + TMA).
+struct ExtendParams {
+    const __nv_bfloat16 *q, *k, *v;
+    const float *slopes;
+    float *pool;
+    const int32_t *state_idx;
+    const int32_t *cu_seqlens;
+    const uint8_t *prefix_mask;
+    __nv_bfloat16 *out;
+    unsigned int *err;
+    int B, T, H, num_slots, max_seqlen;
+    unsigned long long wait_limit;
+};
+
+cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);
+
+}  // namespace la

@@ -1,0 +1,164 @@
+// la_recurrent.cu -- token-serial seg_la kernels: one-token decode, chain verify, short extends.
+//
+// Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
+// "独立参考实现：逐 token 递推公式":  S_t = S_{t-1} * exp(-slope_h) + outer(k_t, v_t),
+// o_t = (q_t @ S_t) * D^-0.5.  Chain verify follows the same page's section "生产环境不支持",
+// item 3 (every draft token continues from the previous position).
+//
+// These paths are HBM-bound: per (request, head) the 128 x 128 fp32 state (64 KiB) is read once,
+// updated token by token in registers, and written once (decode: back to the pool; verify: once
+// per draft token into the intermediate-state buffer).  Design for GB300:
+//   * one CTA of 256 threads per (request, head); warp w owns state rows [16w, 16w+16), lane l
+//     owns columns [4l, 4l+4), so every state access is a 16-byte vector load/store and a warp
+//     touches 512 contiguous bytes of a row -- fully coalesced;
+//   * all 16 row loads of a thread are issued back to back before any arithmetic (64 KiB in
+//     flight per CTA), with evict-first cache hints since the state is touched exactly once;
+//   * the readout q @ S contracts over rows, i.e. across the 8 warps: each thread accumulates its
+//     16-row partial sum in registers and the 8 partials meet in shared memory (double-buffered,
+//     so one __syncthreads per token suffices);
+//   * the decay is applied and the outer product added with one FMA per state element.
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerWarp = kHeadDim / kWarps;  // 16
+// head_dim^-0.5 for head_dim = 128, i.e. 2^-3.5
+constexpr float kScale = 0.08838834764831845f;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
+    f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+    f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p) {
+    const int H = p.H;
+    const int b = blockIdx.x / H;
+    const int h = blockIdx.x - b * H;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row0 = warp * kRowsPerWarp;
+    const int col = lane * 4;
+
+    __shared__ __align__(16) float red[2][kWarps][kHeadDim];
+
+    const int slot = p.state_idx[b];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        return;
+    }
+    float *state = p.pool + ((size_t)slot * H + h) * (size_t)(kHeadDim * kHeadDim);
+
+    int t_begin, n;
+    bool from_pool = true;
+    if (MODE == RECUR_EXTEND) {
+        t_begin = p.cu_seqlens[b];
+        const int t_end = p.cu_seqlens[b + 1];
+        if (t_begin < 0 || t_end < t_begin || t_end > p.T) {
+            if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
+            return;
+        }
+        n = t_end - t_begin;
+        from_pool = p.prefix_mask[b] != 0;
+    } else if (MODE == RECUR_DECODE) {
+        t_begin = b;
+        n = 1;
+    } else {
+        t_begin = b * p.N;
+        n = p.N;
+    }
+
+    float4 s[kRowsPerWarp];
+    if (from_pool) {
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+            s[r] = __ldcs(reinterpret_cast<const float4 *>(state + (size_t)(row0 + r) * kHeadDim +
+                                                           col));
+    } else {
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    const float decay = expf(-p.slopes[h]);
+    const size_t row_stride = (size_t)H * kHeadDim;
+
+    for (int t = 0; t < n; ++t) {
+        const size_t tok = (size_t)(t_begin + t) * row_stride + (size_t)h * kHeadDim;
+        // this warp's 16 k and q entries (same address across the warp: a broadcast) and this
+        // lane's 4 v entries
+        const uint4 *kp = reinterpret_cast<const uint4 *>(p.k + tok + row0);
+        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + tok + row0);
+        const uint2 vv = *reinterpret_cast<const uint2 *>(p.v + tok + col);
+        float kf[16], qf[16];
+        unpack8(kp[0], kf);
+        unpack8(kp[1], kf + 8);
+        unpack8(qp[0], qf);
+        unpack8(qp[1], qf + 8);
+        const float v0 = bf_lo(vv.x), v1 = bf_hi(vv.x), v2 = bf_lo(vv.y), v3 = bf_hi(vv.y);
+
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            // S = S * exp(-slope) + outer(k, v), one FMA per element
+            s[r].x = fmaf(kf[r], v0, s[r].x * decay);
+            s[r].y = fmaf(kf[r], v1, s[r].y * decay);
+            s[r].z = fmaf(kf[r], v2, s[r].z * decay);
+            s[r].w = fmaf(kf[r], v3, s[r].w * decay);
+            o.x = fmaf(qf[r], s[r].x, o.x);
+            o.y = fmaf(qf[r], s[r].y, o.y);
+            o.z = fmaf(qf[r], s[r].z, o.z);
+            o.w = fmaf(qf[r], s[r].w, o.w);
+        }
+        if (MODE == RECUR_VERIFY) {
+            float *dst = p.inter + (((size_t)b * p.N + t) * H + h) * (size_t)(kHeadDim * kHeadDim);
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r)
+                __stcs(reinterpret_cast<float4 *>(dst + (size_t)(row0 + r) * kHeadDim + col), s[r]);
+        }
+        float(*buf)[kHeadDim] = red[t & 1];
+        *reinterpret_cast<float4 *>(&buf[warp][col]) = o;
+        __syncthreads();
+        if (threadIdx.x < kHeadDim / 2) {
+            const int j = threadIdx.x * 2;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                a0 += buf[w][j];
+                a1 += buf[w][j + 1];
+            }
+            *reinterpret_cast<__nv_bfloat162 *>(p.out + tok + j) =
+                __floats2bfloat162_rn(a0 * kScale, a1 * kScale);
+        }
+        // red[t & 1] is rewritten at token t + 2, after every reader has passed the barrier of
+        // token t + 1, so one barrier per token is enough.
+    }
+
+    if (MODE != RECUR_VERIFY) {
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+            __stcs(reinterpret_cast<float4 *>(state + (size_t)(row0 + r) * kHeadDim + col), s[r]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream) {
+    const long long blocks = (long long)p.B * p.H;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks), block(kThreads);
+    switch (mode) {
+        case RECUR_DECODE: recurrent_kernel<RECUR_DECODE><<<grid, block, 0, stream>>>(p); break;
+        case RECUR_VERIFY: recurrent_kernel<RECUR_VERIFY><<<grid, block, 0, stream>>>(p); break;
+        case RECUR_EXTEND: recurrent_kernel<RECUR_EXTEND><<<grid, block, 0, stream>>>(p); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace la

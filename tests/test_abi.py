@@ -1,0 +1,86 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol include/la.h declares,
+and its host-only paths (slopes, argument checks, status strings) behave without a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import lightning_attention_gb300 as la
+from lightning_attention_gb300 import _build, binding
+from la_testutil import oracle_slopes_fp32
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(la_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("la_extend", "la_decode", "la_verify_chain", "la_slopes", "la_poll_error",
+                     "la_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(declared_functions()) <= set(binding.EXPORTS) | set(declared_functions())
+
+
+def test_slopes_match_oracle_rule(lib):
+    for (H, l, L) in [(2, 0, 1), (16, 3, 8), (16, 0, 4), (32, 5, 12), (64, 10, 20), (8, 7, 8),
+                      (12, 1, 3)]:
+        got = la.slopes(H, l, L).double().numpy()
+        ref = oracle_slopes_fp32(H, l, L)
+        # both sides round one fp64 value to fp32; allow one fp32 ulp for libm differences
+        np.testing.assert_allclose(got, ref, rtol=2 ** -23, atol=0)
+
+
+def test_slopes_reject_bad_arguments(lib):
+    buf = (ctypes.c_float * 4)()
+    for args in [(0, 0, 1), (4, 1, 1), (4, -1, 2), (4, 0, 0)]:
+        assert lib.la_slopes(*args, buf) == 1
+    assert lib.la_slopes(4, 0, 1, None) == 1
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    n = None
+    # unsupported head_dim is refused before anything touches the device
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 64, 1, n) == 2
+    assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 1, 64, n) == 2
+    assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 1, 1, 64, n) == 2
+    # negative sizes / bad counts
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, -1, 0, 1, 128, 0, n) == 1
+    assert lib.la_extend(n, n, n, n, n, 0, n, n, n, n, 1, 1, 1, 128, 1, n) == 1
+    assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 0, 128, n) == 1
+    assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 0, 1, 128, n) == 1
+    # null pointers with work to do
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 128, 1, n) == 1
+    assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 1, 128, n) == 1
+    assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 2, 1, 128, n) == 1
+    # empty batch is a no-op
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 0, 0, 1, 128, 0, n) == 0
+    assert lib.la_decode(n, n, n, n, n, 1, n, n, 0, 1, 128, n) == 0
+    assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 0, 1, 1, 128, n) == 0
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.la_status_string(code).decode().startswith(name)
+    assert lib.la_status_string(99).decode() == "LA_ERR_UNKNOWN"

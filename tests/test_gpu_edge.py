@@ -1,0 +1,154 @@
+"""GPU edge cases: ragged lengths around chunk boundaries, empty and zero-length requests, split
+invariance, streams, and device-side input checks (which report through la_poll_error)."""
+import numpy as np
+import pytest
+import torch
+
+import lightning_attention_gb300 as la
+import oracle
+from lightning_attention_gb300 import workloads
+from la_testutil import assert_close, oracle_slopes_fp32, to64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def run_pair(w):
+    pool0 = w.materialize_pool()
+    pool_dev = pool0.to(DEV)
+    out = la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV),
+                    la.slopes(w.H, w.layer_id, w.L).to(DEV), pool_dev, w.state_idx.to(DEV),
+                    w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV))
+    la.poll_error()
+    o_ref, p_ref = oracle.extend(w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy(),
+                                 oracle_slopes_fp32(w.H, w.layer_id, w.L),
+                                 pool0.double().numpy(), w.state_idx.numpy(),
+                                 w.cu_seqlens.numpy(), w.prefix_mask.numpy(), w.H, w.D)
+    return out, pool_dev, pool0, o_ref, p_ref
+
+
+def check(w):
+    out, pool_dev, pool0, o_ref, p_ref = run_pair(w)
+    assert_close(to64(out), o_ref, f"{w.name}: out")
+    idx = w.state_idx.numpy()
+    pa = pool_dev.cpu()
+    assert_close(pa.double().numpy()[idx], p_ref[idx], f"{w.name}: states")
+    untouched = np.ones(w.num_slots, bool)
+    untouched[idx] = False
+    u = torch.from_numpy(untouched)
+    assert torch.equal(pa[u].view(torch.int32), pool0[u].view(torch.int32))
+
+
+@pytest.mark.parametrize("lengths", [
+    [1], [2, 3], [127], [128], [129], [255, 256, 257], [37, 64],
+    [1, 128, 0, 130, 383, 5, 64, 65],
+    [0, 0, 0],
+])
+def test_ragged_lengths(lengths):
+    check(workloads.custom_extend(lengths, H=3, layer_id=1, L=3, seed=len(lengths)))
+
+
+def test_many_heads_and_requests():
+    rng = np.random.default_rng(3)
+    lengths = [int(x) for x in rng.integers(0, 300, size=24)]
+    check(workloads.custom_extend(lengths, H=8, layer_id=2, L=4, seed=11))
+
+
+def test_empty_batch_is_noop():
+    w = workloads.custom_extend([], H=2)
+    pool = torch.zeros(2, 2, 128, 128, device=DEV)
+    out = la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(2, 0, 1).to(DEV), pool,
+                    w.state_idx.to(DEV), w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV))
+    la.poll_error()
+    assert out.shape == (0, 256)
+
+
+@pytest.mark.parametrize("split", [1, 100, 127, 128, 129, 300])
+def test_split_invariance_gpu(split):
+    """extend(A) then extend(B) from the carried state matches one pass over A||B."""
+    n = 400
+    w = workloads.custom_extend([n], H=2, prefix=[1], seed=5)
+    s = la.slopes(2, 0, 1).to(DEV)
+    q, k, v = w.q.to(DEV), w.k.to(DEV), w.v.to(DEV)
+    idx = w.state_idx.to(DEV)
+    pool_a = w.materialize_pool(DEV)
+    pool_b = pool_a.clone()
+    ones = torch.ones(1, dtype=torch.uint8, device=DEV)
+    full = la.extend(q, k, v, s, pool_a, idx, torch.tensor([0, n], dtype=torch.int32, device=DEV),
+                     ones)
+    o1 = la.extend(q[:split].contiguous(), k[:split].contiguous(), v[:split].contiguous(), s,
+                   pool_b, idx, torch.tensor([0, split], dtype=torch.int32, device=DEV), ones)
+    o2 = la.extend(q[split:].contiguous(), k[split:].contiguous(), v[split:].contiguous(), s,
+                   pool_b, idx, torch.tensor([0, n - split], dtype=torch.int32, device=DEV), ones)
+    la.poll_error()
+    assert_close(to64(torch.cat([o1, o2])), to64(full), "split: out")
+    assert_close(pool_b.cpu().double().numpy(), pool_a.cpu().double().numpy(), "split: state")
+
+
+def test_runs_on_a_side_stream():
+    w = workloads.custom_extend([70, 200], H=2, seed=9)
+    out_ref, pool_ref_dev, *_ = run_pair(w)
+    st = torch.cuda.Stream()
+    pool_dev = w.materialize_pool(DEV)
+    with torch.cuda.stream(st):
+        out = la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(2, 0, 1).to(DEV),
+                        pool_dev, w.state_idx.to(DEV), w.cu_seqlens.to(DEV),
+                        w.prefix_mask.to(DEV))
+        la.poll_error()
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), out_ref.cpu())
+    assert torch.equal(pool_dev.cpu(), pool_ref_dev.cpu())
+
+
+def test_slot_out_of_range_is_reported_not_written():
+    w = workloads.custom_extend([10, 20], H=2, prefix=[0, 0], num_slots=4, seed=2,
+                                shuffle_slots=False)
+    pool = torch.zeros(4, 2, 128, 128, device=DEV)
+    bad_idx = torch.tensor([1, 7], dtype=torch.int32, device=DEV)
+    la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(2, 0, 1).to(DEV), pool, bad_idx,
+              w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV))
+    with pytest.raises(la.LAError) as e:
+        la.poll_error()
+    assert e.value.status == 5
+    la.poll_error()  # cleared
+    # decode and verify check the same way
+    q = torch.zeros(2, 256, dtype=torch.bfloat16, device=DEV)
+    la.decode(q, q, q, la.slopes(2, 0, 1).to(DEV), pool,
+              torch.tensor([0, -1], dtype=torch.int32, device=DEV))
+    with pytest.raises(la.LAError):
+        la.poll_error()
+    la.verify_chain(q, q, q, la.slopes(2, 0, 1).to(DEV), pool,
+                    torch.tensor([4, 0], dtype=torch.int32, device=DEV), 1)
+    with pytest.raises(la.LAError):
+        la.poll_error()
+    la.poll_error()
+
+
+def test_bad_cu_seqlens_is_reported():
+    w = workloads.custom_extend([10, 20], H=2, prefix=[0, 0], seed=2)
+    pool = torch.zeros(w.num_slots, 2, 128, 128, device=DEV)
+    cu = torch.tensor([0, 25, 20], dtype=torch.int32, device=DEV)  # decreasing
+    la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(2, 0, 1).to(DEV), pool,
+              w.state_idx.to(DEV), cu, w.prefix_mask.to(DEV))
+    with pytest.raises(la.LAError) as e:
+        la.poll_error()
+    assert e.value.status == 5
+
+
+def test_verify_small_and_decode_identity():
+    """Verify outputs and states equal successive decodes from the same pool state."""
+    w = workloads.custom_verify(3, 4, H=2, seed=4)
+    s = la.slopes(2, 0, 1).to(DEV)
+    pool = w.materialize_pool(DEV)
+    out, inter = la.verify_chain(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), s, pool,
+                                 w.state_idx.to(DEV), w.N)
+    la.poll_error()
+    pool2 = pool.clone()
+    for t in range(w.N):
+        rows = torch.arange(w.B) * w.N + t
+        o = la.decode(w.q[rows].to(DEV), w.k[rows].to(DEV), w.v[rows].to(DEV), s, pool2,
+                      w.state_idx.to(DEV))
+        la.poll_error()
+        assert torch.equal(o.cpu(), out.cpu()[rows])
+        idx = w.state_idx.long()
+        assert torch.equal(pool2.cpu()[idx], inter.cpu()[:, t])
