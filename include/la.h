@@ -22,6 +22,8 @@
  *   - Only head_dim D = 128 is supported (LA_ERR_UNSUPPORTED otherwise), in the spirit of the
  *     head-dim entry guards the page's section "输入与配置覆盖" describes.  q, k and v share one
  *     head count H (no grouped-query heads), as the same section states for seg_la.
+ *   - Device pointers to q, k, v, out and state_pool must be 16-byte aligned (the extend kernel
+ *     moves them with TMA and 16-byte vector accesses); LA_ERR_INVALID otherwise.
  *   - Pointers marked "device" must be device memory of the current CUDA device (or managed
  *     memory); "host" pointers are host memory.  The caller owns every buffer; the library keeps
  *     no pointer after a call returns and allocates no device memory.
@@ -150,12 +152,14 @@ la_status la_poll_error(la_stream stream);
 const char *la_status_string(la_status status);
 
 /*
- * la_set_wait_limit -- diagnostics: the number of polls after which a device wait in the extend
- * kernel gives up, sets the error word and lets the kernel exit cleanly (0 restores the default,
- * which is far above any legitimate wait).  Host only; affects later launches from this process.
- * Lets a test drive the timeout path without hanging or faulting the GPU.
+ * la_set_wait_limit -- diagnostics: how long (in microseconds) a device wait inside the extend
+ * kernel may last before it gives up, sets the error word (LA_ERR_TIMEOUT from la_poll_error)
+ * and lets the kernel exit cleanly: the CTA waits for its own copies and MMAs in flight, frees
+ * its tensor memory and returns, leaving the context usable.  0 restores the default (2 s, far
+ * above any legitimate wait).  Host only; applies to later launches from this process.  Lets a
+ * test drive the timeout path without hanging or faulting the GPU.
  */
-void la_set_wait_limit(uint64_t polls);
+void la_set_wait_limit(uint64_t microseconds);
 
 #ifdef __cplusplus
 }

@@ -23,9 +23,11 @@ std::mutex g_mutex;
 unsigned int *g_err_ptr[kMaxDevices] = {nullptr};
 std::atomic<unsigned long long> g_wait_limit{0};
 
-// Far above any legitimate wait (each poll is a try_wait with a hardware time hint), small enough
-// that a lost arrival ends the kernel in about a second instead of hanging the GPU.
-constexpr unsigned long long kDefaultWaitLimit = 1ull << 22;
+// Default bound on a device wait: far above any legitimate wait inside one CTA (microseconds),
+// short enough that a lost arrival ends the kernel in about two seconds instead of hanging.
+constexpr unsigned long long kDefaultWaitLimitUs = 2000000ull;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 la_status error_word_ptr(unsigned int **out) {
     int dev = 0;
@@ -71,7 +73,7 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out) {
     return LA_OK;
 }
 
-void la_set_wait_limit(uint64_t polls) { g_wait_limit.store(polls); }
+void la_set_wait_limit(uint64_t microseconds) { g_wait_limit.store(microseconds); }
 
 la_status la_poll_error(la_stream stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -158,10 +160,12 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     if (!slopes || !state_pool || !state_idx || !cu_seqlens || !prefix_mask) return LA_ERR_INVALID;
     if (T > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID;
     if ((long long)T * H * D >= (1ll << 40)) return LA_ERR_UNSUPPORTED;
+    if (!aligned16(state_pool) || (T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+                                             !aligned16(out))))
+        return LA_ERR_INVALID;
     la_status st;
-    unsigned int *err = nullptr;
-    if ((st = error_word_ptr(&err)) != LA_OK) return st;
-    la::RecurParams p{};
+    la::ExtendParams p{};
+    if ((st = error_word_ptr(&p.err)) != LA_OK) return st;
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
     p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
@@ -171,12 +175,14 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     p.cu_seqlens = cu_seqlens;
     p.prefix_mask = prefix_mask;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.err = err;
     p.B = B;
-    p.H = H;
     p.T = T;
+    p.H = H;
     p.num_slots = num_slots;
-    return launch_status(la::launch_recurrent(la::RECUR_EXTEND, p, static_cast<cudaStream_t>(stream)));
+    p.max_seqlen = max_seqlen;
+    const unsigned long long us = g_wait_limit.load();
+    p.wait_limit_ns = (us == 0 ? kDefaultWaitLimitUs : us) * 1000ull;
+    return launch_status(la::launch_extend_chunked(p, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,554 @@
+// la_extend_tc.cu -- chunked seg_la extend on the 5th-generation tensor cores (tcgen05 + TMA).
+//
+// Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
+// "独立参考实现：逐 token 递推公式": per head, S_t = S_{t-1} e^{-s} + outer(k_t, v_t) and
+// o_t = (q_t @ S_t) D^-0.5, over each request's tokens, from the request's pool state (or zero),
+// final state written back.
+//
+// Chunked form (exact up to rounding; the recurrence unrolled over a chunk of r <= C tokens, with
+// local token indices i, j in [0, r) and S the state before the chunk):
+//   o_i    = D^-0.5 gamma_i (Q S)_i  +  ((Q K^T o Dm) D^-0.5 V)_i,
+//            gamma_i = e^{-s (i+1)},  Dm_ij = e^{-s (i-j)} if j <= i, else 0
+//   S_next = e^{-s r} S  +  K^T diag(lambda) V,       lambda_j = e^{-s (r-1-j)}
+// Every decay factor is <= 1 and is built directly from its exponent, never as a ratio of two
+// exponentials (e^{-s i} / e^{-s j} overflows for s*C large).
+//
+// One CTA owns one (request b, head h, v-column block of DV = 64) and walks the request's chunks
+// of C = 128 tokens in order.  Roles (320 threads):
+//   warp 8      TMA producer: Q, K (C x 128) and the V block (C x 64) of each chunk into a
+//               two-stage ring (128-byte swizzled tiles, one mbarrier per stage);
+//   warp 9      TMEM allocator and MMA issuer (one thread), all accumulating in fp32:
+//                 MMA1  A_c      = Q K^T                      bf16 x bf16  (M=N=K=128)
+//                 MMA2  Oint_c   = Q S_hi + Q S_lo            bf16 x bf16  (M=128, N=64, K=128)
+//                 MMA3  Ointra_c = P V                        fp16 x fp16  (K = 128 tokens)
+//                 MMA4  U_c      = (lambda K)^T V             fp16 x fp16  (M=128 k-dims, N=64)
+//   warps 0-7   epilogue (TMEM lane quarter = warp % 4; the two warpgroups split columns):
+//                 mask  P = A o Dm D^-0.5 -> fp16 in shared memory; V converted to fp16 and K
+//                       scaled by lambda into fp16, in place (after MMA1 has consumed K);
+//                 state S = e^{-s r} S + U in fp32 registers (the master copy), written to
+//                       shared memory as S_hi = bf16(S), S_lo = bf16(S - S_hi) for MMA2;
+//                 out   o = gamma D^-0.5 Oint + Ointra -> bf16 -> global.
+// Precision: Q and K enter MMA1 exactly (bf16 inputs); the state operand is split hi + lo, so
+// Q S carries about 16 bits of the fp32 state; P, V and lambda K are fp16 (11-bit significand,
+// 4x finer than bf16); everything accumulates in fp32.
+// TMEM (512 columns): A double-buffered (2 x 128), Oint (64), Ointra (64), U (64).
+// MMA1 of chunk c+1 is issued before MMA2-4 of chunk c, so the QK^T product of the next chunk
+// overlaps the epilogue of the current one; TMA runs up to two chunks ahead.
+//
+// Buffer reuse needs no extra barriers: the epilogue handles chunk c in the order mask, state,
+// out and signals p_ready(c+1) only after out(c) has read Oint/Ointra; the MMA issuer issues
+// MMA1 of chunk c+2 (which overwrites A[c % 2]) and MMA2-4 of chunk c+1 only after p_ready(c+1)
+// or p_ready(c) respectively, i.e. after the epilogue is done with the buffers they overwrite.
+//
+// Every mbarrier wait is bounded (a globaltimer deadline).  A wait that runs out sets the error
+// word and an abort flag; every role then leaves its loop, the producer waits for its own copies
+// in flight and the MMA issuer for its MMAs, and the CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "la_internal.h"
+#include "la_sm100.cuh"
+
+namespace la {
+namespace {
+
+using namespace sm100;
+
+constexpr int C = 128;              // chunk length in tokens
+constexpr int DV = 64;              // v columns per CTA
+constexpr int NV = kHeadDim / DV;   // v blocks per head
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_A = 0;        // 2 x 128 columns
+constexpr uint32_t TM_OI = 256;     // DV columns: Q S
+constexpr uint32_t TM_OP = 320;     // DV columns: P V
+constexpr uint32_t TM_U = 384;      // DV columns
+// head_dim^-0.5 for head_dim = 128, i.e. 2^-3.5
+constexpr float kScale = 0.08838834764831845f;
+
+// Shared memory (offsets from a 1024-byte aligned base).  Tiles are 128-byte swizzled; a
+// [rows][128] 16-bit tile is two [rows][64] blocks 16 KiB apart.
+constexpr uint32_t SZ_QK = C * kHeadDim * 2;        // 32 KiB
+constexpr uint32_t SZ_V = C * DV * 2;               // 16 KiB
+constexpr uint32_t SZ_STAGE = 2 * SZ_QK + SZ_V;     // Q, K, V of one chunk
+constexpr uint32_t OFF_P = 2 * SZ_STAGE;
+constexpr uint32_t SZ_P = C * C * 2;
+constexpr uint32_t OFF_SHI = OFF_P + SZ_P;
+constexpr uint32_t SZ_S = kHeadDim * DV * 2;
+constexpr uint32_t OFF_SLO = OFF_SHI + SZ_S;
+constexpr uint32_t OFF_TAB = OFF_SLO + SZ_S;        // e^{-s m}, m = 0..C
+constexpr uint32_t OFF_TABP = OFF_TAB + 544;        // e^{-s m} D^-0.5, m = 0..C
+constexpr uint32_t OFF_BAR = OFF_TABP + 544;
+constexpr uint32_t SZ_BAR = 192;
+constexpr uint32_t kSmemBytes = OFF_BAR + SZ_BAR + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(OFF_BAR % 8 == 0, "barrier alignment");
+static_assert(SZ_STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_SHI % 1024 == 0 &&
+                  OFF_SLO % 1024 == 0,
+              "operand tiles start on 1024-byte swizzle atoms");
+constexpr uint32_t kStageTxBytes = SZ_STAGE;
+
+struct Bars {
+    uint64_t full[2];    // TMA -> MMA: stage loaded
+    uint64_t empty[2];   // MMA -> TMA: stage consumed (MMA4 of the chunk done)
+    uint64_t a_full[2];  // MMA1 done
+    uint64_t o_full;     // MMA2 + MMA3 done
+    uint64_t u_full;     // MMA4 done
+    uint64_t p_ready;    // epilogue: P written, V and K converted, previous O read (8 arrivals)
+    uint64_t s_ready;    // epilogue: S_hi/S_lo written, U read (8 arrivals)
+    uint64_t drain;      // MMA issuer: all MMAs done
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= SZ_BAR, "barrier block");
+
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                         volatile int *abort_flag, unsigned int *err) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_BIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// All 32 lanes wait (each acquires the barrier); the warp proceeds only if every lane succeeded.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, unsigned int *err) {
+    const bool ok = wait_bar(bar, parity, limit_ns, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {
+    // K-major operand, 128 x 128 tile as two 64-column blocks: 16 K elements per MMA.
+    return sdesc_sw128(tile + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk, uint32_t lbo) {
+    // MN-major operand (rows = contraction index): 16 rows (two 8-row groups) per MMA.
+    return sdesc_sw128(tile + (uint32_t)kk * 2048u, lbo, 1024);
+}
+
+// Convert 64 bf16 values (one 128-byte row of a swizzled block) to fp16 times f, in place.  The
+// swizzle only permutes 16-byte chunks within the row, so an elementwise map ignores it.
+__device__ __forceinline__ void row64_bf16_to_f16(uint8_t *row, float f) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint4 *pp = reinterpret_cast<uint4 *>(row + ch * 16);
+        const uint4 x = *pp;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f,
+                              __uint_as_float(w[e] & 0xffff0000u) * f);
+        *pp = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Write this thread's 32 state columns (one row of the [128 k-dims][DV] tile) as bf16 hi and lo.
+__device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, int row, int wg,
+                                                  const float *S) {
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = S[k4 * 8 + 2 * e], b = S[k4 * 8 + 2 * e + 1];
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            const float2 hf = __bfloat1622float2(h);
+            hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+            lo[e] = pack_bf16x2(a - hf.x, b - hf.y);
+        }
+        const int off = row * 128 + (((wg * 4 + k4) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(s_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_chunked_kernel(const __grid_constant__ CUtensorMap tq,
+                          const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv, const ExtendParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+    float *tab = reinterpret_cast<float *>(sm + OFF_TAB);
+    float *tabp = reinterpret_cast<float *>(sm + OFF_TABP);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = p.H;
+    const int vb = blockIdx.x % NV;
+    const int bh = blockIdx.x / NV;
+    const int h = bh % H;
+    const int b = bh / H;
+
+    // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
+    const int slot = p.state_idx[b];
+    const int t0 = p.cu_seqlens[b];
+    const int t1 = p.cu_seqlens[b + 1];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        return;
+    }
+    if (t0 < 0 || t1 < t0 || t1 > p.T) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
+        return;
+    }
+    const int n = t1 - t0;
+    const int nchunks = (n + C - 1) / C;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->a_full[s], 1);
+        }
+        mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->u_full, 1);
+        mbar_init(&bars->p_ready, kEpiWarps);
+        mbar_init(&bars->s_ready, kEpiWarps);
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0 && nchunks > 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int *abort_flag = &bars->abort_flag;
+
+    const uint32_t s_base = smem_u32(sm);
+    auto sQ = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE; };
+    auto sK = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE + SZ_QK; };
+    auto sV = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE + 2 * SZ_QK; };
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1;
+                if (c >= 2 &&
+                    !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                const int y = t0 + c * C;
+                const int xq = h * kHeadDim;
+                uint8_t *dst = sm + st * SZ_STAGE;
+                mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
+                tma_load_2d(dst, &tq, &bars->full[st], xq, y);
+                tma_load_2d(dst + 16384, &tq, &bars->full[st], xq + 64, y);
+                tma_load_2d(dst + SZ_QK, &tk, &bars->full[st], xq, y);
+                tma_load_2d(dst + SZ_QK + 16384, &tk, &bars->full[st], xq + 64, y);
+                tma_load_2d(dst + 2 * SZ_QK, &tv, &bars->full[st], xq + vb * DV, y);
+                issued = c + 1;
+            }
+            // Copies still in flight must land before the CTA's shared memory goes away.
+            for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
+                int dummy = 0;
+                wait_bar(&bars->full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idA = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t idI = idesc_bf16_f32(128, DV, false, true);
+            const uint32_t idP = idesc_f16_f32(128, DV, false, true);
+            const uint32_t idU = idesc_f16_f32(128, DV, true, true);
+            const uint32_t sP = s_base + OFF_P;
+            const uint32_t sHi = s_base + OFF_SHI;
+            const uint32_t sLo = s_base + OFF_SLO;
+            bool ok = true;
+            auto issue_qk = [&](int c) -> bool {
+                const int st = c & 1;
+                if (!wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err))
+                    return false;
+                tc_fence_after();
+                const uint32_t dA = tbase + TM_A + (uint32_t)st * 128u;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(dA, kdesc(sQ(st), kk), kdesc(sK(st), kk), idA, kk > 0);
+                mma_commit(&bars->a_full[st]);
+                return true;
+            };
+            if (nchunks > 0) ok = issue_qk(0);
+            for (int c = 0; c < nchunks && ok; ++c) {
+                if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
+                const int st = c & 1;
+                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err) ||
+                    !wait_bar(&bars->s_ready, c & 1, limit, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // Oint = Q S_hi
+                    mma_bf16(tbase + TM_OI, kdesc(sQ(st), kk), mndesc(sHi, kk, 8192), idI, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // Oint += Q S_lo
+                    mma_bf16(tbase + TM_OI, kdesc(sQ(st), kk), mndesc(sLo, kk, 8192), idI, 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // Ointra = P V
+                    mma_bf16(tbase + TM_OP, kdesc(sP, kk), mndesc(sV(st), kk, 8192), idP, kk > 0);
+                mma_commit(&bars->o_full);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // U = (lambda K)^T V
+                    mma_bf16(tbase + TM_U, mndesc(sK(st), kk, 16384), mndesc(sV(st), kk, 8192),
+                             idU, kk > 0);
+                mma_commit(&bars->u_full);
+                mma_commit(&bars->empty[st]);
+            }
+            // Every issued MMA must finish before TMEM is freed.
+            mma_commit(&bars->drain);
+            int dummy = 0;
+            wait_bar(&bars->drain, 0, kDrainLimitNs, &dummy, p.err);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue warps
+        const int wg = warp >> 2;          // column half
+        const int q = warp & 3;            // TMEM lane quarter
+        const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (U, S)
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int col0 = vb * DV + wg * 32;  // first v column this thread owns
+
+        const float slope = p.slopes[h];
+        for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
+            const float e = expf(-slope * (float)m);
+            tab[m] = e;
+            tabp[m] = e * kScale;
+        }
+        {
+            uint4 *P4 = reinterpret_cast<uint4 *>(sm + OFF_P);
+            for (int x = threadIdx.x; x < (int)(SZ_P / 16); x += kEpiThreads)
+                P4[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        float S[32];
+        float *gstate =
+            p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
+        if (p.prefix_mask[b]) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float4 f = *reinterpret_cast<const float4 *>(gstate + 4 * x);
+                S[4 * x] = f.x;
+                S[4 * x + 1] = f.y;
+                S[4 * x + 2] = f.z;
+                S[4 * x + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) S[x] = 0.f;
+        }
+        uint8_t *s_hi = sm + OFF_SHI;
+        uint8_t *s_lo = sm + OFF_SLO;
+        store_state_split(s_hi, s_lo, i, wg, S);
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables + P zeros
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_ready);
+
+        const size_t row_stride = (size_t)H * kHeadDim;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1;
+            const int r = min(C, n - c * C);
+
+            // ---- mask: P = A o Dm D^-0.5 (fp16); V -> fp16; K -> lambda K (fp16)
+            if (!(ok = warp_wait_bar(&bars->a_full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
+                break;
+            tc_fence_after();
+            for (int cb = wg; cb <= q; cb += 2) {
+                uint32_t v[32];
+                tmem_ld32(tbase + lane_off + TM_A + (uint32_t)st * 128u + (uint32_t)cb * 32u, v);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const int d0 = i - (cb * 32 + jj);
+                    const float x0 = d0 >= 0 ? __uint_as_float(v[jj]) * tabp[d0] : 0.f;
+                    const float x1 = d0 >= 1 ? __uint_as_float(v[jj + 1]) * tabp[d0 - 1] : 0.f;
+                    pk[jj >> 1] = pack_f16x2(x0, x1);
+                }
+                uint8_t *prow = sm + OFF_P + (cb >> 1) * 16384 + i * 128;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int chunk = ((cb & 1) * 4 + k4) ^ (i & 7);
+                    *reinterpret_cast<uint4 *>(prow + chunk * 16) =
+                        make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+                }
+            }
+            if (wg == 0) {
+                row64_bf16_to_f16(sm + st * SZ_STAGE + 2 * SZ_QK + i * 128, 1.f);
+            } else {
+                const float lam = i < r ? tab[r - 1 - i] : 0.f;
+                uint8_t *krow = sm + st * SZ_STAGE + SZ_QK + i * 128;
+                row64_bf16_to_f16(krow, lam);
+                row64_bf16_to_f16(krow + 16384, lam);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_ready);
+
+            // ---- state: S = e^{-s r} S + U (fp32 master in registers), hi/lo copy for MMA2
+            if (!(ok = warp_wait_bar(&bars->u_full, c & 1, limit, abort_flag, p.err))) break;
+            tc_fence_after();
+            {
+                uint32_t v[32];
+                tmem_ld32(tbase + lane_off + TM_U + (uint32_t)wg * 32u, v);
+                tmem_ld_wait();
+                const float dr = tab[r];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) S[x] = fmaf(S[x], dr, __uint_as_float(v[x]));
+                store_state_split(s_hi, s_lo, i, wg, S);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_ready);
+
+            // ---- out: o = gamma D^-0.5 Oint + Ointra -> bf16
+            if (!(ok = warp_wait_bar(&bars->o_full, c & 1, limit, abort_flag, p.err))) break;
+            tc_fence_after();
+            {
+                uint32_t vi[32], vp[32];
+                tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)wg * 32u, vi);
+                tmem_ld32(tbase + lane_off + TM_OP + (uint32_t)wg * 32u, vp);
+                tmem_ld_wait();
+                tc_fence_before();
+                if (i < r) {
+                    const float g = tabp[i + 1];
+                    __nv_bfloat16 *dst =
+                        p.out + (size_t)(t0 + c * C + i) * row_stride + (size_t)h * kHeadDim + col0;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int x = k4 * 8 + 2 * e;
+                            w[e] = pack_bf16x2(
+                                fmaf(g, __uint_as_float(vi[x]), __uint_as_float(vp[x])),
+                                fmaf(g, __uint_as_float(vi[x + 1]), __uint_as_float(vp[x + 1])));
+                        }
+                        *reinterpret_cast<uint4 *>(dst + k4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+        // Final state write-back (also for zero-length requests).  Skipped after an abort: the
+        // error word already reports the failure.
+        if (ok && !*abort_flag) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                *reinterpret_cast<float4 *>(gstate + 4 * x) =
+                    make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// [T][H*128] bf16, box of 64 columns x C rows, 128-byte swizzle; rows past T read as zero.
+bool make_token_map(CUtensorMap *m, const void *ptr, int T, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)C};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream) {
+    const long long units = (long long)p.B * p.H * NV;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    CUtensorMap tq, tk, tv;
+    memset(&tq, 0, sizeof(tq));
+    memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv));
+    if (p.T > 0) {
+        if (!make_token_map(&tq, p.q, p.T, p.H) || !make_token_map(&tk, p.k, p.T, p.H) ||
+            !make_token_map(&tv, p.v, p.T, p.H))
+            return cudaErrorInvalidValue;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {false};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev]) {
+            e = cudaFuncSetAttribute(extend_chunked_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    extend_chunked_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -45,7 +45,7 @@ struct ExtendParams {
     __nv_bfloat16 *out;
     unsigned int *err;
     int B, T, H, num_slots, max_seqlen;
-    unsigned long long wait_limit;
+    unsigned long long wait_limit_ns;  // bound on every mbarrier wait
 };
 
 cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);
