@@ -16,29 +16,33 @@
 // One CTA owns one (request b, head h, v-column block of DV = 64) and walks the request's chunks
 // of C = 128 tokens in order.  Roles (320 threads):
 //   warp 8      TMA producer: Q, K (C x 128) and the V block (C x 64) of each chunk into a
-//               two-stage ring (128-byte swizzled tiles, one mbarrier per stage);
+//               two-stage ring (128-byte swizzled tiles, one mbarrier per stage); the whole warp
+//               then converts the landed V tile to fp16 in place, off the epilogue's path;
 //   warp 9      TMEM allocator and MMA issuer (one thread), all accumulating in fp32:
 //                 MMA1  A_c      = Q K^T                      bf16 x bf16  (M=N=K=128)
 //                 MMA2  Oint_c   = Q S_hi + Q S_lo            bf16 x bf16  (M=128, N=64, K=128)
 //                 MMA3  Ointra_c = P V                        fp16 x fp16  (K = 128 tokens)
 //                 MMA4  U_c      = (lambda K)^T V             fp16 x fp16  (M=128 k-dims, N=64)
 //   warps 0-7   epilogue (TMEM lane quarter = warp % 4; the two warpgroups split columns):
-//                 mask  P = A o Dm D^-0.5 -> fp16 in shared memory; V converted to fp16 and K
-//                       scaled by lambda into fp16, in place (after MMA1 has consumed K);
-//                 state S = e^{-s r} S + U in fp32 registers (the master copy), written to
+//                 mask  P = A o Dm D^-0.5 -> fp16 in shared memory (lower-triangular blocks
+//                       only; the upper ones stay zero), and K scaled by lambda into fp16 in
+//                       place once MMA1 has consumed it (each warpgroup one 64-column half);
+//                 state S = e^{-s r} S + U in fp32 (the master copy, in TMEM), written to
 //                       shared memory as S_hi = bf16(S), S_lo = bf16(S - S_hi) for MMA2;
 //                 out   o = gamma D^-0.5 Oint + Ointra -> bf16 -> global.
 // Precision: Q and K enter MMA1 exactly (bf16 inputs); the state operand is split hi + lo, so
 // Q S carries about 16 bits of the fp32 state; P, V and lambda K are fp16 (11-bit significand,
 // 4x finer than bf16); everything accumulates in fp32.
-// TMEM (512 columns): A double-buffered (2 x 128), Oint (64), Ointra (64), U (64).
-// MMA1 of chunk c+1 is issued before MMA2-4 of chunk c, so the QK^T product of the next chunk
-// overlaps the epilogue of the current one; TMA runs up to two chunks ahead.
+// TMEM (512 columns): A double-buffered (2 x 128), Oint (64), Ointra (64), U (64) and the fp32
+// master state S (64), kept in tensor memory rather than registers.
 //
-// Buffer reuse needs no extra barriers: the epilogue handles chunk c in the order mask, state,
-// out and signals p_ready(c+1) only after out(c) has read Oint/Ointra; the MMA issuer issues
-// MMA1 of chunk c+2 (which overwrites A[c % 2]) and MMA2-4 of chunk c+1 only after p_ready(c+1)
-// or p_ready(c) respectively, i.e. after the epilogue is done with the buffers they overwrite.
+// Issue order for chunk c: MMA2_c as soon as the previous state is written (s_ready) and the
+// previous outputs have been read (o_free); MMA4_c then MMA3_c once the mask pass (p_ready) and
+// the fp16 V tile (v_ready) are in; then MMA1_{c+1}.  The epilogue handles chunk c as mask,
+// state, out.  Reuse of the other buffers follows from these orders: MMA1_{c+1} overwrites the
+// A buffer of chunk c-1 after p_ready(c); the mask pass of chunk c+1 rewrites P after out(c) has
+// waited for MMA3_c; state(c) rewrites S_hi/S_lo after u_full(c), which by issue order also
+// covers MMA2_c; MMA4_c overwrites U after s_ready(c), i.e. after state(c-1) has read it.
 //
 // Every mbarrier wait is bounded (a globaltimer deadline).  A wait that runs out sets the error
 // word and an abort flag; every role then leaves its loop, the producer waits for its own copies
@@ -69,6 +73,7 @@ constexpr uint32_t TM_A = 0;        // 2 x 128 columns
 constexpr uint32_t TM_OI = 256;     // DV columns: Q S
 constexpr uint32_t TM_OP = 320;     // DV columns: P V
 constexpr uint32_t TM_U = 384;      // DV columns
+constexpr uint32_t TM_S = 448;      // DV columns: the fp32 master state
 // head_dim^-0.5 for head_dim = 128, i.e. 2^-3.5
 constexpr float kScale = 0.08838834764831845f;
 
@@ -95,14 +100,16 @@ static_assert(SZ_STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_SHI % 1024 == 0 &
 constexpr uint32_t kStageTxBytes = SZ_STAGE;
 
 struct Bars {
-    uint64_t full[2];    // TMA -> MMA: stage loaded
-    uint64_t empty[2];   // MMA -> TMA: stage consumed (MMA4 of the chunk done)
-    uint64_t a_full[2];  // MMA1 done
-    uint64_t o_full;     // MMA2 + MMA3 done
-    uint64_t u_full;     // MMA4 done
-    uint64_t p_ready;    // epilogue: P written, V and K converted, previous O read (8 arrivals)
-    uint64_t s_ready;    // epilogue: S_hi/S_lo written, U read (8 arrivals)
-    uint64_t drain;      // MMA issuer: all MMAs done
+    uint64_t full[2];     // TMA -> all: stage loaded
+    uint64_t empty[2];    // MMA -> TMA: stage consumed (MMA3/MMA4 of the chunk done)
+    uint64_t a_full[2];   // MMA1 done
+    uint64_t v_ready[2];  // producer warp: V tile converted to fp16
+    uint64_t p_ready;     // epilogue: P written, K scaled (8 warp arrivals)
+    uint64_t s_ready;     // epilogue: S_hi/S_lo written, U read (8)
+    uint64_t o_free;      // epilogue: Oint/Ointra read (8)
+    uint64_t u_full;      // MMA4 done (and, by issue order, MMA2 of the same chunk)
+    uint64_t o_full;      // MMA3 done (and MMA2 of the same chunk)
+    uint64_t drain;       // MMA issuer: all MMAs done
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -133,31 +140,22 @@ __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, ui
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {
-    // K-major operand, 128 x 128 tile as two 64-column blocks: 16 K elements per MMA.
-    return sdesc_sw128(tile + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u, 16, 1024);
+// Descriptor offsets (in the 16-byte units of the start-address field) of the kk-th 16-deep
+// slice of the contraction: K-major 128 x 128 tiles are two 64-column blocks 16 KiB apart, each
+// slice 32 bytes into the 128-byte row; MN-major tiles advance 16 rows (2 KiB) per slice.
+__device__ __forceinline__ uint64_t kofs(int kk) {
+    return (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
 }
+__device__ __forceinline__ uint64_t mnofs(int kk) { return (uint64_t)(kk * 128); }
 
-__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk, uint32_t lbo) {
-    // MN-major operand (rows = contraction index): 16 rows (two 8-row groups) per MMA.
-    return sdesc_sw128(tile + (uint32_t)kk * 2048u, lbo, 1024);
-}
-
-// Convert 64 bf16 values (one 128-byte row of a swizzled block) to fp16 times f, in place.  The
-// swizzle only permutes 16-byte chunks within the row, so an elementwise map ignores it.
-__device__ __forceinline__ void row64_bf16_to_f16(uint8_t *row, float f) {
+// 16-byte chunk: 8 bf16 -> 8 fp16 times f.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x, float f) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4 *pp = reinterpret_cast<uint4 *>(row + ch * 16);
-        const uint4 x = *pp;
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f,
-                              __uint_as_float(w[e] & 0xffff0000u) * f);
-        *pp = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    for (int e = 0; e < 4; ++e)
+        o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Write this thread's 32 state columns (one row of the [128 k-dims][DV] tile) as bf16 hi and lo.
@@ -177,6 +175,37 @@ __device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, 
         const int off = row * 128 + (((wg * 4 + k4) ^ (row & 7)) << 4);
         *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(s_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// P row segment: 32 columns of block cb of row i, decay-masked and scaled, as fp16.  Below the
+// diagonal block (cb < i / 32) every i - j >= 1, so no mask is needed; in the diagonal block the
+// table is read at a clamped index and the upper triangle selected away afterwards (the loads stay
+// unconditional, which keeps the code branch-free).
+__device__ __forceinline__ void store_p_block(uint8_t *sP, int i, int cb, const uint32_t (&v)[32],
+                                              const float *tabp) {
+    uint32_t pk[16];
+    const int d = i - cb * 32;  // i - j for jj = 0
+    if (d >= 32) {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2)
+            pk[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * tabp[d - jj],
+                                     __uint_as_float(v[jj + 1]) * tabp[d - jj - 1]);
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2) {
+            const int d0 = d - jj, d1 = d - jj - 1;
+            const float x0 = __uint_as_float(v[jj]) * tabp[max(d0, 0)];
+            const float x1 = __uint_as_float(v[jj + 1]) * tabp[max(d1, 0)];
+            pk[jj >> 1] = pack_f16x2(d0 >= 0 ? x0 : 0.f, d1 >= 0 ? x1 : 0.f);
+        }
+    }
+    uint8_t *prow = sP + (cb >> 1) * 16384 + i * 128;
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const int chunk = ((cb & 1) * 4 + k4) ^ (i & 7);
+        *reinterpret_cast<uint4 *>(prow + chunk * 16) =
+            make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
     }
 }
 
@@ -221,11 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
             mbar_init(&bars->a_full[s], 1);
+            mbar_init(&bars->v_ready[s], 1);
         }
-        mbar_init(&bars->o_full, 1);
-        mbar_init(&bars->u_full, 1);
         mbar_init(&bars->p_ready, kEpiWarps);
         mbar_init(&bars->s_ready, kEpiWarps);
+        mbar_init(&bars->o_free, kEpiWarps);
+        mbar_init(&bars->u_full, 1);
+        mbar_init(&bars->o_full, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -246,31 +277,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = &bars->abort_flag;
 
     const uint32_t s_base = smem_u32(sm);
-    auto sQ = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE; };
-    auto sK = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE + SZ_QK; };
-    auto sV = [&](int st) { return s_base + (uint32_t)st * SZ_STAGE + 2 * SZ_QK; };
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1;
-                if (c >= 2 &&
-                    !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
-                    break;
-                const int y = t0 + c * C;
-                const int xq = h * kHeadDim;
-                uint8_t *dst = sm + st * SZ_STAGE;
-                mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
-                tma_load_2d(dst, &tq, &bars->full[st], xq, y);
-                tma_load_2d(dst + 16384, &tq, &bars->full[st], xq + 64, y);
-                tma_load_2d(dst + SZ_QK, &tk, &bars->full[st], xq, y);
-                tma_load_2d(dst + SZ_QK + 16384, &tk, &bars->full[st], xq + 64, y);
-                tma_load_2d(dst + 2 * SZ_QK, &tv, &bars->full[st], xq + vb * DV, y);
-                issued = c + 1;
+        // ------------------------------------------------------------ TMA producer + V to fp16
+        int issued = 0;  // meaningful in lane 0
+        auto issue = [&](int c) -> bool {
+            const int st = c & 1;
+            if (c >= 2 &&
+                !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                return false;
+            const int y = t0 + c * C;
+            const int xq = h * kHeadDim;
+            uint8_t *dst = sm + st * SZ_STAGE;
+            mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
+            tma_load_2d(dst, &tq, &bars->full[st], xq, y);
+            tma_load_2d(dst + 16384, &tq, &bars->full[st], xq + 64, y);
+            tma_load_2d(dst + SZ_QK, &tk, &bars->full[st], xq, y);
+            tma_load_2d(dst + SZ_QK + 16384, &tk, &bars->full[st], xq + 64, y);
+            tma_load_2d(dst + 2 * SZ_QK, &tv, &bars->full[st], xq + vb * DV, y);
+            issued = c + 1;
+            return true;
+        };
+        int ok = 1;
+        if (lane == 0 && nchunks > 0) ok = issue(0);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        for (int c = 0; c < nchunks && ok; ++c) {
+            if (lane == 0 && c + 1 < nchunks) ok = issue(c + 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int st = c & 1;
+            if (!(ok = warp_wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
+                break;
+            // the whole 16 KiB V tile, 16-byte chunks, 32 consecutive chunks per instruction
+            uint4 *vt = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + 2 * SZ_QK);
+            for (int m0 = 0; m0 < (int)(SZ_V / 16 / 32); m0 += 8) {
+                uint4 vbuf[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) vbuf[m] = vt[lane + 32 * (m0 + m)];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) vt[lane + 32 * (m0 + m)] = bf16x8_to_f16x8(vbuf[m], 1.f);
             }
-            // Copies still in flight must land before the CTA's shared memory goes away.
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->v_ready[st]);
+        }
+        // Copies still in flight must land before the CTA's shared memory goes away.
+        if (lane == 0) {
             for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
                 int dummy = 0;
                 wait_bar(&bars->full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
@@ -283,10 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idI = idesc_bf16_f32(128, DV, false, true);
             const uint32_t idP = idesc_f16_f32(128, DV, false, true);
             const uint32_t idU = idesc_f16_f32(128, DV, true, true);
-            const uint32_t sP = s_base + OFF_P;
-            const uint32_t sHi = s_base + OFF_SHI;
-            const uint32_t sLo = s_base + OFF_SLO;
-            bool ok = true;
+            // Stage st's descriptors are stage 0's plus st * SZ_STAGE in the address field.
+            const uint64_t dQ0 = sdesc_sw128(s_base, 16, 1024);
+            const uint64_t dK0 = sdesc_sw128(s_base + SZ_QK, 16, 1024);
+            const uint64_t dKt0 = sdesc_sw128(s_base + SZ_QK, 16384, 1024);
+            const uint64_t dV0 = sdesc_sw128(s_base + 2 * SZ_QK, 8192, 1024);
+            const uint64_t stage_step = SZ_STAGE >> 4;
+            const uint64_t dP = sdesc_sw128(s_base + OFF_P, 16, 1024);
+            const uint64_t dHi = sdesc_sw128(s_base + OFF_SHI, 8192, 1024);
+            const uint64_t dLo = sdesc_sw128(s_base + OFF_SLO, 8192, 1024);
             auto issue_qk = [&](int c) -> bool {
                 const int st = c & 1;
                 if (!wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err))
@@ -295,36 +352,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dA = tbase + TM_A + (uint32_t)st * 128u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(dA, kdesc(sQ(st), kk), kdesc(sK(st), kk), idA, kk > 0);
+                    mma_bf16(dA, dQ0 + st * stage_step + kofs(kk), dK0 + st * stage_step + kofs(kk), idA, kk > 0);
                 mma_commit(&bars->a_full[st]);
                 return true;
             };
+            bool ok = true;
             if (nchunks > 0) ok = issue_qk(0);
             for (int c = 0; c < nchunks && ok; ++c) {
-                if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
                 const int st = c & 1;
-                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err) ||
-                    !wait_bar(&bars->s_ready, c & 1, limit, abort_flag, p.err)) {
+                // Oint = Q S_{c-1}: needs the previous state and the previous outputs read
+                if (!wait_bar(&bars->s_ready, c & 1, limit, abort_flag, p.err) ||
+                    (c >= 1 && !wait_bar(&bars->o_free, (c - 1) & 1, limit, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Oint = Q S_hi
-                    mma_bf16(tbase + TM_OI, kdesc(sQ(st), kk), mndesc(sHi, kk, 8192), idI, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dHi + mnofs(kk), idI, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Oint += Q S_lo
-                    mma_bf16(tbase + TM_OI, kdesc(sQ(st), kk), mndesc(sLo, kk, 8192), idI, 1);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dLo + mnofs(kk), idI, 1);
+                // U = (lambda K)^T V and Ointra = P V: need the mask pass and the fp16 V tile
+                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err) ||
+                    !wait_bar(&bars->v_ready[st], (c >> 1) & 1, limit, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Ointra = P V
-                    mma_bf16(tbase + TM_OP, kdesc(sP, kk), mndesc(sV(st), kk, 8192), idP, kk > 0);
-                mma_commit(&bars->o_full);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // U = (lambda K)^T V
-                    mma_bf16(tbase + TM_U, mndesc(sK(st), kk, 16384), mndesc(sV(st), kk, 8192),
-                             idU, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_U, dKt0 + st * stage_step + mnofs(kk), dV0 + st * stage_step + mnofs(kk), idU, kk > 0);
                 mma_commit(&bars->u_full);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_OP, dP + kofs(kk), dV0 + st * stage_step + mnofs(kk), idP, kk > 0);
+                mma_commit(&bars->o_full);
                 mma_commit(&bars->empty[st]);
+                if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
             }
             // Every issued MMA must finish before TMEM is freed.
             mma_commit(&bars->drain);
@@ -333,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue warps
-        const int wg = warp >> 2;          // column half
+        const int wg = warp >> 2;          // column half / K block
         const int q = warp & 3;            // TMEM lane quarter
         const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (U, S)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -350,67 +415,80 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = threadIdx.x; x < (int)(SZ_P / 16); x += kEpiThreads)
                 P4[x] = make_uint4(0u, 0u, 0u, 0u);
         }
-        float S[32];
         float *gstate =
             p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
-        if (p.prefix_mask[b]) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float4 f = *reinterpret_cast<const float4 *>(gstate + 4 * x);
-                S[4 * x] = f.x;
-                S[4 * x + 1] = f.y;
-                S[4 * x + 2] = f.z;
-                S[4 * x + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) S[x] = 0.f;
-        }
+        const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)wg * 32u;
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
-        store_state_split(s_hi, s_lo, i, wg, S);
+        uint8_t *sP = sm + OFF_P;
+        {
+            float S[32];
+            if (p.prefix_mask[b]) {
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 f = *reinterpret_cast<const float4 *>(gstate + 4 * x);
+                    S[4 * x] = f.x;
+                    S[4 * x + 1] = f.y;
+                    S[4 * x + 2] = f.z;
+                    S[4 * x + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) S[x] = 0.f;
+            }
+            uint32_t w[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[x]);
+            tmem_st32(t_s, w);
+            store_state_split(s_hi, s_lo, i, wg, S);
+            tmem_st_wait();
+        }
         fence_proxy_async_smem();
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables + P zeros
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_ready);
 
+        // P blocks of this warp: column blocks wg and wg + 2 of its lane quarter, where on or
+        // below the diagonal (block cb > q is all zero and never written).
+        const bool blk_a = q >= wg;
+        const bool blk_b = q >= wg + 2;
         const size_t row_stride = (size_t)H * kHeadDim;
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
             const int r = min(C, n - c * C);
 
-            // ---- mask: P = A o Dm D^-0.5 (fp16); V -> fp16; K -> lambda K (fp16)
+            // ---- mask: P = A o Dm D^-0.5 (fp16); K row half -> lambda K (fp16)
             if (!(ok = warp_wait_bar(&bars->a_full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
                 break;
             tc_fence_after();
-            for (int cb = wg; cb <= q; cb += 2) {
-                uint32_t v[32];
-                tmem_ld32(tbase + lane_off + TM_A + (uint32_t)st * 128u + (uint32_t)cb * 32u, v);
-                tmem_ld_wait();
-                uint32_t pk[16];
+            {
+                uint32_t va[32];
+                const uint32_t ta = tbase + lane_off + TM_A + (uint32_t)st * 128u;
+                if (blk_a) tmem_ld32(ta + (uint32_t)wg * 32u, va);
+                // K row i, 64-column block wg, scaled by lambda_i while the TMEM load flies;
+                // chunk order rotated by row so that 8 consecutive rows hit 8 distinct banks
+                {
+                    const float lam = i < r ? tab[r - 1 - i] : 0.f;
+                    uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_QK +
+                                                            wg * 16384 + i * 128);
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
-                    const int d0 = i - (cb * 32 + jj);
-                    const float x0 = d0 >= 0 ? __uint_as_float(v[jj]) * tabp[d0] : 0.f;
-                    const float x1 = d0 >= 1 ? __uint_as_float(v[jj + 1]) * tabp[d0 - 1] : 0.f;
-                    pk[jj >> 1] = pack_f16x2(x0, x1);
-                }
-                uint8_t *prow = sm + OFF_P + (cb >> 1) * 16384 + i * 128;
+                    for (int h4 = 0; h4 < 8; h4 += 4) {
+                        uint4 kbuf[4];
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int chunk = ((cb & 1) * 4 + k4) ^ (i & 7);
-                    *reinterpret_cast<uint4 *>(prow + chunk * 16) =
-                        make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+                        for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + i) & 7];
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            krow[(h4 + ch + i) & 7] = bf16x8_to_f16x8(kbuf[ch], lam);
+                    }
                 }
-            }
-            if (wg == 0) {
-                row64_bf16_to_f16(sm + st * SZ_STAGE + 2 * SZ_QK + i * 128, 1.f);
-            } else {
-                const float lam = i < r ? tab[r - 1 - i] : 0.f;
-                uint8_t *krow = sm + st * SZ_STAGE + SZ_QK + i * 128;
-                row64_bf16_to_f16(krow, lam);
-                row64_bf16_to_f16(krow + 16384, lam);
+                tmem_ld_wait_regs(va);
+                if (blk_a) store_p_block(sP, i, wg, va, tabp);
+                if (blk_b) {
+                    tmem_ld32(ta + (uint32_t)(wg + 2) * 32u, va);
+                    tmem_ld_wait_regs(va);
+                    store_p_block(sP, i, wg + 2, va, tabp);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -421,13 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->u_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
             {
-                uint32_t v[32];
+                uint32_t v[32], w[32];
                 tmem_ld32(tbase + lane_off + TM_U + (uint32_t)wg * 32u, v);
-                tmem_ld_wait();
+                tmem_ld32(t_s, w);
+                tmem_ld_wait_regs2(v, w);
                 const float dr = tab[r];
+                float S[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) S[x] = fmaf(S[x], dr, __uint_as_float(v[x]));
+                for (int x = 0; x < 32; ++x) {
+                    S[x] = fmaf(__uint_as_float(w[x]), dr, __uint_as_float(v[x]));
+                    w[x] = __float_as_uint(S[x]);
+                }
+                tmem_st32(t_s, w);
                 store_state_split(s_hi, s_lo, i, wg, S);
+                tmem_st_wait();
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -441,8 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t vi[32], vp[32];
                 tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)wg * 32u, vi);
                 tmem_ld32(tbase + lane_off + TM_OP + (uint32_t)wg * 32u, vp);
-                tmem_ld_wait();
+                tmem_ld_wait_regs2(vi, vp);
                 tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->o_free);
                 if (i < r) {
                     const float g = tabp[i + 1];
                     __nv_bfloat16 *dst =
@@ -465,10 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Final state write-back (also for zero-length requests).  Skipped after an abort: the
         // error word already reports the failure.
         if (ok && !*abort_flag) {
+            uint32_t w[32];
+            tmem_ld32(t_s, w);
+            tmem_ld_wait_regs(w);
 #pragma unroll
             for (int x = 0; x < 8; ++x)
                 *reinterpret_cast<float4 *>(gstate + 4 * x) =
-                    make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+                    make_float4(__uint_as_float(w[4 * x]), __uint_as_float(w[4 * x + 1]),
+                                __uint_as_float(w[4 * x + 2]), __uint_as_float(w[4 * x + 3]));
         }
     }
 
