@@ -530,21 +530,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->o_free);
-                if (i < r) {
-                    const float g = tabp[i + 1];
-                    __nv_bfloat16 *dst =
-                        p.out + (size_t)(t0 + c * C + i) * row_stride + (size_t)h * kHeadDim + col0;
+                // o = gamma D^-0.5 Oint + Ointra for this thread's row, packed to 4 x 16 bytes
+                const float g = tabp[i + 1];
+                uint4 ch[4];
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        uint32_t w[4];
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int x = k4 * 8 + 2 * e;
-                            w[e] = pack_bf16x2(
-                                fmaf(g, __uint_as_float(vi[x]), __uint_as_float(vp[x])),
-                                fmaf(g, __uint_as_float(vi[x + 1]), __uint_as_float(vp[x + 1])));
-                        }
-                        *reinterpret_cast<uint4 *>(dst + k4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int x = k4 * 8 + 2 * e;
+                        w[e] = pack_bf16x2(
+                            fmaf(g, __uint_as_float(vi[x]), __uint_as_float(vp[x])),
+                            fmaf(g, __uint_as_float(vi[x + 1]), __uint_as_float(vp[x + 1])));
+                    }
+                    ch[k4] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                // 4x4 transpose of 16-byte chunks within each group of 4 lanes (two butterfly
+                // steps), so that store k writes row 4*(lane/4) + k of the group as one contiguous
+                // 64-byte segment per group: 8 full segments per instruction instead of 32
+                // scattered 16-byte pieces.
+                const int pq = lane & 3;
+                {
+                    const bool lo2 = pq < 2;
+                    uint4 sa = lo2 ? ch[2] : ch[0], sb = lo2 ? ch[3] : ch[1];
+                    uint4 ra, rb;
+                    ra.x = __shfl_xor_sync(0xffffffffu, sa.x, 2);
+                    ra.y = __shfl_xor_sync(0xffffffffu, sa.y, 2);
+                    ra.z = __shfl_xor_sync(0xffffffffu, sa.z, 2);
+                    ra.w = __shfl_xor_sync(0xffffffffu, sa.w, 2);
+                    rb.x = __shfl_xor_sync(0xffffffffu, sb.x, 2);
+                    rb.y = __shfl_xor_sync(0xffffffffu, sb.y, 2);
+                    rb.z = __shfl_xor_sync(0xffffffffu, sb.z, 2);
+                    rb.w = __shfl_xor_sync(0xffffffffu, sb.w, 2);
+                    if (lo2) { ch[2] = ra; ch[3] = rb; } else { ch[0] = ra; ch[1] = rb; }
+                }
+                {
+                    const bool even = (pq & 1) == 0;
+                    uint4 sa = even ? ch[1] : ch[0], sb = even ? ch[3] : ch[2];
+                    uint4 ra, rb;
+                    ra.x = __shfl_xor_sync(0xffffffffu, sa.x, 1);
+                    ra.y = __shfl_xor_sync(0xffffffffu, sa.y, 1);
+                    ra.z = __shfl_xor_sync(0xffffffffu, sa.z, 1);
+                    ra.w = __shfl_xor_sync(0xffffffffu, sa.w, 1);
+                    rb.x = __shfl_xor_sync(0xffffffffu, sb.x, 1);
+                    rb.y = __shfl_xor_sync(0xffffffffu, sb.y, 1);
+                    rb.z = __shfl_xor_sync(0xffffffffu, sb.z, 1);
+                    rb.w = __shfl_xor_sync(0xffffffffu, sb.w, 1);
+                    if (even) { ch[1] = ra; ch[3] = rb; } else { ch[0] = ra; ch[2] = rb; }
+                }
+                // lane (4 g + pq) now holds chunk pq of rows 4 g .. 4 g + 3 of its warp's 32 rows
+                const int rbase = q * 32 + (lane & ~3);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = rbase + k;
+                    if (row < r) {
+                        __nv_bfloat16 *dst = p.out + (size_t)(t0 + c * C + row) * row_stride +
+                                             (size_t)h * kHeadDim + col0 + pq * 8;
+                        *reinterpret_cast<uint4 *>(dst) = ch[k];
                     }
                 }
             }
