@@ -243,11 +243,17 @@ class GpuCase:
         self.pool = w.materialize_pool(dev)
         self.idx = w.state_idx.to(dev)
         self.out = torch.empty_like(self.q)
+        self.launches_per_step = 1
+        self.kernel = KERNEL_NAME[{"decode": "decode", "verify": "verify"}.get(w.kind, "varlen_extend")]
         if w.kind == "extend":
             self.cu = w.cu_seqlens.to(dev)
             self.pm = w.prefix_mask.to(dev)
             lens = w.cu_seqlens[1:] - w.cu_seqlens[:-1]
             self.max_seqlen = int(lens.max()) if w.B else 0
+            if la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen) > 0:
+                # long requests split into segments: block-state kernel, then the extend kernel
+                self.launches_per_step = 2
+                self.kernel = "block_state_kernel + extend_chunked_kernel (one la_extend call)"
         if w.kind == "verify":
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
 
@@ -296,15 +302,17 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
     la.poll_error()
     dev_s = ev0.elapsed_time(ev1) / 1e3
     max_s = max_over_ranks(dev_s, world, dev)
-    per_launch = dev_s / steps                      # one launch of the dominant kernel per step
+    per_launch = dev_s / steps  # one la_extend / la_decode / la_verify_chain call per step
     value = aggregate_throughput(geo["tokens"], steps, world, max_s)
 
     achieved_gbs = geo["bytes"] / per_launch / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
             "traffic": stored_traffic(name), "peak_source": peaks["source"],
-            "algorithmic_bytes_per_launch": geo["bytes"], "kernel": KERNEL_NAME[name],
+            "algorithmic_bytes_per_launch": geo["bytes"], "kernel": case.kernel,
             "launch_ms": round(per_launch * 1e3, 4)}
+    if case.launches_per_step > 1:
+        roof["traffic"] = None  # ncu traffic is recorded for single-kernel calls only
     tensor = None
     if w.kind == "extend":
         tflops = geo["flops"] / per_launch / 1e12
@@ -316,6 +324,7 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
     if with_e2e:
         e2e = time_e2e(case, w, geo, steps, world, dev)
     res = {"value": value, "ms_per_step": max_s / steps * 1e3, "tokens_per_step": geo["tokens"],
+           "gpu_launches": steps * case.launches_per_step,
            "roofline": roof, "wall_s": wall1 - wall0, "clocks": clocks, "e2e": e2e,
            "workload": w, "geo": geo}
     if tensor:
@@ -502,7 +511,7 @@ def main():
             "dtype": "f32" if w.kind != "extend" else "bf16",
             "data": "synthetic (seeded; see lightning_attention_gb300/workloads.py)",
             "config": workload_config(args.workload, w, world),
-            "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": args.steps,
+            "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
             "clocks": head["clocks"]}
     if "tensor" in head:
         line["tensor"] = head["tensor"]
@@ -523,7 +532,7 @@ def main():
                          with_e2e=False, sampler=None)
             entry = {"workload": r["workload"].name, "value": r["value"], "unit": "tokens/s",
                      "steps": steps, "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
-                     "gpu_launches": steps}
+                     "gpu_launches": r["gpu_launches"]}
             if "tensor" in r:
                 entry["tensor"] = r["tensor"]
             others.append(entry)

@@ -43,6 +43,7 @@
 #ifndef LA_GB300_H
 #define LA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -93,15 +94,34 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *                (the slot is then never read)
  *   out          device, bf16 [T][H*D], written
  *   B, T, H, D   requests, total tokens (= cu_seqlens[B]), heads, head_dim (must be 128)
- *   max_seqlen   an upper bound on every request's length (T is always a valid value)
+ *   max_seqlen   an upper bound on every request's length (T is always a valid value); it and
+ *                B, H decide the schedule (see la_extend_workspace_size)
+ *   workspace    device scratch of workspace_bytes bytes (16-byte aligned), or NULL.  When the
+ *                batch has too few (request, head) pairs to fill the GPU, long requests are cut
+ *                into segments processed in parallel; that needs la_extend_workspace_size()
+ *                bytes of scratch.  With NULL or a smaller buffer the call runs unsplit (same
+ *                results up to rounding, fewer CTAs).  The caller owns it; its contents on entry
+ *                do not matter and are garbage on exit; calls sharing one workspace must not
+ *                overlap on the GPU.
+ *   workspace_bytes  size of workspace
  *   stream       cudaStream_t
- * Numerics: bf16 inputs; fp32 states and accumulation; the intra-chunk products run on the
- * tensor cores with bf16 operands and fp32 accumulators; out is rounded to bf16 once.
+ * Numerics: bf16 inputs; fp32 states and accumulation; Q K^T runs on the tensor cores in bf16,
+ * the state operand of Q S in two bf16 halves (hi + lo), P V and K^T V in fp16, all accumulating
+ * in fp32; out is rounded to bf16 once.
  */
 la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
                     float *state_pool, int num_slots, const int32_t *state_idx,
                     const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
-                    int T, int H, int D, int max_seqlen, la_stream stream);
+                    int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
+                    la_stream stream);
+
+/*
+ * la_extend_workspace_size -- bytes of device scratch la_extend would use for a batch of this
+ * shape on the current device (0 when it would not split any request).  Host only, no device work
+ * beyond one cached attribute query.  Arguments as for la_extend; *bytes is written on success.
+ * Returns LA_ERR_INVALID for negative sizes or bytes == NULL, LA_ERR_UNSUPPORTED for D != 128.
+ */
+la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, size_t *bytes);
 
 /*
  * la_decode -- one decode token per request, state updated in place.

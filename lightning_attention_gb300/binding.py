@@ -23,8 +23,8 @@ _lib = None
 STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
           4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
 
-EXPORTS = ("la_slopes", "la_extend", "la_decode", "la_verify_chain", "la_poll_error",
-           "la_status_string", "la_set_wait_limit")
+EXPORTS = ("la_slopes", "la_extend", "la_extend_workspace_size", "la_decode", "la_verify_chain",
+           "la_poll_error", "la_status_string", "la_set_wait_limit")
 
 
 class LAError(RuntimeError):
@@ -53,8 +53,12 @@ def load():
         vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_float)
         lib.la_slopes.argtypes = [ip, ip, ip, fp]
         lib.la_slopes.restype = ip
-        lib.la_extend.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp]
+        sz = ctypes.c_size_t
+        lib.la_extend.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp, sz,
+                                  vp]
         lib.la_extend.restype = ip
+        lib.la_extend_workspace_size.argtypes = [ip, ip, ip, ip, ip, ctypes.POINTER(sz)]
+        lib.la_extend_workspace_size.restype = ip
         lib.la_decode.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, vp]
         lib.la_decode.restype = ip
         lib.la_verify_chain.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, ip, ip, ip, ip, vp]
@@ -113,10 +117,35 @@ def poll_error(device=None) -> None:
     _check("la_poll_error", load().la_poll_error(_stream_handle(dev)))
 
 
+_ws_cache: dict = {}
+
+
+def extend_workspace_size(B: int, T: int, H: int, D: int, max_seqlen: int) -> int:
+    """Bytes of scratch la_extend uses for this batch shape on the current device (0: none)."""
+    n = ctypes.c_size_t(0)
+    _check("la_extend_workspace_size",
+           load().la_extend_workspace_size(B, T, H, D, max_seqlen, ctypes.byref(n)))
+    return int(n.value)
+
+
+def _cached_workspace(dev: torch.device, nbytes: int) -> torch.Tensor:
+    # one growing scratch buffer per device, shared by calls on that device: calls that use it
+    # on different streams concurrently must pass their own workspace instead
+    t = _ws_cache.get(dev.index)
+    if t is None or t.numel() < nbytes:
+        t = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        _ws_cache[dev.index] = t
+    return t
+
+
 def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
-           max_seqlen: int | None = None):
+           max_seqlen: int | None = None, workspace=None):
     """Packed varlen extend (la_extend).  q, k, v: bf16 [T, H*D]; state_pool fp32
-    [S, H, D, D] updated in place; returns out bf16 [T, H*D]."""
+    [S, H, D, D] updated in place; returns out bf16 [T, H*D].
+
+    workspace: None lets the binding supply the scratch la_extend_workspace_size asks for (a
+    cached per-device buffer); False runs without scratch (no sequence split); a uint8 CUDA
+    tensor is used as given."""
     dev = q.device
     T = q.shape[0]
     num_slots, H, D, D2 = state_pool.shape
@@ -134,9 +163,19 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     if max_seqlen is None:
         max_seqlen = T
     with torch.cuda.device(dev):
+        if workspace is None:
+            nbytes = extend_workspace_size(B, T, H, D, int(max_seqlen))
+            ws = _cached_workspace(dev, nbytes) if nbytes > 0 else None
+        elif workspace is False:
+            ws = None
+        else:
+            ws = workspace
+            _need(ws, "workspace", torch.uint8, dev)
+        ws_ptr = _ptr(ws)
+        ws_bytes = ws.numel() if ws is not None else 0
         st = load().la_extend(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool), num_slots,
                               _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask), _ptr(out), B, T,
-                              H, D, int(max_seqlen), _stream_handle(dev))
+                              H, D, int(max_seqlen), ws_ptr, ws_bytes, _stream_handle(dev))
     _check("la_extend", st)
     return out
 

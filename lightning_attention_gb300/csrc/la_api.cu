@@ -45,6 +45,23 @@ la_status error_word_ptr(unsigned int **out) {
 
 la_status launch_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
+int g_num_sms[kMaxDevices] = {0};
+
+la_status num_sms(int *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return LA_ERR_CUDA;
+        g_num_sms[dev] = n;
+    }
+    *out = g_num_sms[dev];
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -152,7 +169,8 @@ la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
 la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
                     float *state_pool, int num_slots, const int32_t *state_idx,
                     const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
-                    int T, int H, int D, int max_seqlen, la_stream stream) {
+                    int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
+                    la_stream stream) {
     if (B < 0 || T < 0 || H < 1 || D < 1 || num_slots < 1 || max_seqlen < 0)
         return LA_ERR_INVALID;
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
@@ -182,7 +200,42 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     p.max_seqlen = max_seqlen;
     const unsigned long long us = g_wait_limit.load();
     p.wait_limit_ns = (us == 0 ? kDefaultWaitLimitUs : us) * 1000ull;
-    return launch_status(la::launch_extend_chunked(p, static_cast<cudaStream_t>(stream)));
+    p.seg_len = 0;
+    p.blk_len = 0;
+    p.nseg = 1;
+    p.nblk = 0;
+    p.ws = nullptr;
+    if (workspace != nullptr && aligned16(workspace) && T > 0) {
+        int sms = 0;
+        if ((st = num_sms(&sms)) != LA_OK) return st;
+        const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms);
+        if (pl.seg_len > 0 && (unsigned long long)workspace_bytes >= pl.ws_bytes) {
+            p.seg_len = pl.seg_len;
+            p.blk_len = pl.blk_len;
+            p.nseg = pl.nseg;
+            p.nblk = pl.nblk;
+            p.ws = static_cast<float *>(workspace);
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.seg_len > 0) {
+        const cudaError_t e = la::launch_block_states(p, s);
+        if (e != cudaSuccess) return LA_ERR_CUDA;
+    }
+    return launch_status(la::launch_extend_chunked(p, s));
+}
+
+la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, size_t *bytes) {
+    if (B < 0 || T < 0 || H < 1 || D < 1 || max_seqlen < 0 || bytes == nullptr)
+        return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    *bytes = 0;
+    if (B == 0 || T == 0) return LA_OK;
+    int sms = 0;
+    la_status st = num_sms(&sms);
+    if (st != LA_OK) return st;
+    *bytes = (size_t)la::plan_split(B, H, max_seqlen, sms).ws_bytes;
+    return LA_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,329 @@
+// la_extend_seg.cu -- sequence split of long extend requests: the split planner and the
+// block-state kernel.
+//
+// Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
+// "独立参考实现：逐 token 递推公式": S_t = S_{t-1} e^{-s} + outer(k_t, v_t).  Unrolled over a block
+// of tokens [a, e) starting from zero, the state at the block's end is
+//     B = sum_{t in [a, e)} e^{-s (e - 1 - t)} outer(k_t, v_t),
+// and the state at any later token boundary x is e^{-s (x - e)} B plus the contributions of the
+// tokens after e.  So a request can be cut into segments processed in parallel: segment g starts
+// from e^{-s x_g} S0 + sum over the blocks k before x_g of e^{-s (x_g - e_k)} B_k (positions
+// relative to the request's first token).  That is a reassociation of the same sum, exact up to
+// rounding.
+//
+// The block-state kernel computes B_k for the blocks that precede a request's last segment, and
+// copies each split request's initial state S0 (its pool slot, or zero) into the workspace, so
+// that the extend kernel's segments never read a pool slot that the last segment rewrites.
+//
+// One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
+// two stages); eight warps scale K by e^{-s (e - 1 - t)} and convert K and V to fp16 in place; one
+// thread issues tcgen05.mma (fp16 x fp16 -> fp32) accumulating B = K_hat^T V in tensor memory over
+// the whole block; the eight warps then write B (fp32, 64 KiB) to the workspace.  The work is HBM
+// bound (64 KiB of K and V per 128 tokens, 2 x 128 x 128 x 128 MMA flops).
+#include <cuda.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "la_internal.h"
+#include "la_sm100.cuh"
+
+namespace la {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int C = 128;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t SZ_T = C * kHeadDim * 2;   // one [C][128] 16-bit tile: two 16 KiB blocks
+constexpr uint32_t SZ_STAGE = 2 * SZ_T;       // K and V of one chunk
+constexpr uint32_t OFF_BAR = 2 * SZ_STAGE;
+constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;
+static_assert(SZ_STAGE % 1024 == 0, "atoms");
+
+struct Bars {
+    uint64_t full[2];   // TMA -> converters
+    uint64_t conv[2];   // converters -> MMA (8 warp arrivals)
+    uint64_t empty[2];  // MMA -> TMA
+    uint64_t done;      // every MMA of the block completed
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= 128, "barrier block");
+
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                         volatile int *abort_flag, unsigned int *err) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_BIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, unsigned int *err) {
+    const bool ok = wait_bar(bar, parity, limit_ns, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x, float f) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    block_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const ExtendParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = p.H;
+    const int k = blockIdx.x % p.nblk;
+    const int bh = blockIdx.x / p.nblk;
+    const int h = bh % H;
+    const int b = bh / H;
+
+    const int slot = p.state_idx[b];
+    const int t0 = p.cu_seqlens[b];
+    const int t1 = p.cu_seqlens[b + 1];
+    if (slot < 0 || slot >= p.num_slots || t0 < 0 || t1 < t0 || t1 > p.T) return;  // the extend
+    // kernel, launched next on the same stream, records these faults in the error word
+    const int n = t1 - t0;
+    const int nseg_b = (n + p.seg_len - 1) / p.seg_len;
+    if (nseg_b <= 1) return;  // not split
+    const int per_seg = p.seg_len / p.blk_len;
+    float *ws_bh = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) * (kHeadDim * kHeadDim);
+
+    // The initial state S0 of a split request (pool slot if it has a prefix, else zero).
+    if (k == 0 && threadIdx.x < kConvThreads) {
+        const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+        const float *src =
+            p.pool + (((size_t)slot * H + h) * kHeadDim + row) * kHeadDim + half * 64;
+        float *dst = ws_bh + (size_t)row * kHeadDim + half * 64;
+        const bool pre = p.prefix_mask[b] != 0;
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+            reinterpret_cast<float4 *>(dst)[x] =
+                pre ? reinterpret_cast<const float4 *>(src)[x] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (k >= (nseg_b - 1) * per_seg) return;  // block at or after the last segment's start
+
+    const int a = k * p.blk_len;               // block [a, e) relative to t0; always full length
+    const int nchunks = p.blk_len / C;
+    const uint64_t limit = p.wait_limit_ns;
+    const float slope = p.slopes[h];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->conv[s], kConvWarps);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->done, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int *abort_flag = &bars->abort_flag;
+    const uint32_t s_base = smem_u32(sm);
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1;
+                if (c >= 2 &&
+                    !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                const int y = t0 + a + c * C;
+                const int x = h * kHeadDim;
+                uint8_t *dst = sm + st * SZ_STAGE;
+                mbar_arrive_expect_tx(&bars->full[st], SZ_STAGE);
+                tma_load_2d(dst, &tk, &bars->full[st], x, y);
+                tma_load_2d(dst + 16384, &tk, &bars->full[st], x + 64, y);
+                tma_load_2d(dst + SZ_T, &tv, &bars->full[st], x, y);
+                tma_load_2d(dst + SZ_T + 16384, &tv, &bars->full[st], x + 64, y);
+                issued = c + 1;
+            }
+            for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
+                int dummy = 0;
+                wait_bar(&bars->full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idU = idesc_f16_f32(128, 64, true, true);
+            const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);        // K^T: MN-major A
+            const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 8192, 1024);  // V half: MN-major B
+            const uint64_t step = SZ_STAGE >> 4;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1;
+                if (!wait_bar(&bars->conv[st], (c >> 1) & 1, limit, abort_flag, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tbase + (uint32_t)half * 64u,
+                                 dK0 + st * step + (uint64_t)(kk * 128),
+                                 dV0 + st * step + (uint64_t)(half * 1024 + kk * 128), idU,
+                                 (c > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars->empty[st]);
+            }
+            mma_commit(&bars->done);
+            int dummy = 0;
+            wait_bar(&bars->done, 0, kDrainLimitNs, &dummy, p.err);
+        }
+    } else {
+        // converters / epilogue: thread pair (2 row, 2 row + 1) owns row `row` of the chunk; each
+        // converts one 64-column half of K and of V
+        const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1;
+            if (!(ok = warp_wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
+                break;
+            // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
+            const float lam = expf(-slope * (float)(p.blk_len - 1 - c * C - row));
+            uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
+            uint4 *vrow =
+                reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_T + half * 16384 + row * 128);
+            const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
+            uint4 kb[8], vb[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) kb[ch] = krow[(ch + rot) & 7];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) vb[ch] = vrow[(ch + rot) & 7];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) krow[(ch + rot) & 7] = bf16x8_to_f16x8(kb[ch], lam);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) vrow[(ch + rot) & 7] = bf16x8_to_f16x8(vb[ch], 1.f);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->conv[st]);
+        }
+        if (ok && warp_wait_bar(&bars->done, 0, limit, abort_flag, p.err)) {
+            tc_fence_after();
+            const int q = warp & 3, wg = warp >> 2;
+            const int i = q * 32 + lane;
+            float *dst = ws_bh + (size_t)(1 + k) * (kHeadDim * kHeadDim) + (size_t)i * kHeadDim +
+                         wg * 64;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(wg * 64 + hh * 32), v);
+                tmem_ld_wait_regs(v);
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    reinterpret_cast<float4 *>(dst + hh * 32)[x] =
+                        make_float4(__uint_as_float(v[4 * x]), __uint_as_float(v[4 * x + 1]),
+                                    __uint_as_float(v[4 * x + 2]), __uint_as_float(v[4 * x + 3]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+}  // namespace
+
+// Split only when the batch leaves SMs idle: with u = B * H * 2 extend CTAs (two v blocks per
+// head) and u < num_sms / 2, cut each request into G = floor(num_sms / u) segments (at least
+// 8 chunks each), and each segment into P blocks so that the block-state kernel also fills the
+// GPU.  Workspace: B * H * (1 + nblk) fp32 D x D matrices.
+SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms) {
+    SplitPlan pl{0, 0, 1, 0, 0ull};
+    const long long units = (long long)B * H * 2;
+    if (B <= 0 || units <= 0 || num_sms <= 0 || 2 * units > num_sms) return pl;
+    const int min_seg = 8 * C;
+    int G = (int)(num_sms / units);
+    const int by_len = max_seqlen / min_seg;
+    if (by_len < G) G = by_len;
+    if (G < 2) return pl;
+    const int seg0 = (max_seqlen + G - 1) / G;
+    const long long bh = (long long)B * H;
+    int P = (int)(num_sms / (bh * (G - 1)));
+    const int p_len = (seg0 + min_seg - 1) / min_seg;
+    if (P > p_len) P = p_len;
+    if (P < 1) P = 1;
+    const int blk = ((seg0 + P - 1) / P + C - 1) / C * C;
+    pl.blk_len = blk;
+    pl.seg_len = blk * P;
+    pl.nseg = (max_seqlen + pl.seg_len - 1) / pl.seg_len;
+    if (pl.nseg < 2) return SplitPlan{0, 0, 1, 0, 0ull};
+    pl.nblk = (pl.nseg - 1) * P;
+    pl.ws_bytes = (unsigned long long)bh * (unsigned long long)(1 + pl.nblk) * kHeadDim * kHeadDim *
+                  sizeof(float);
+    return pl;
+}
+
+bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);  // la_extend_tc.cu
+
+cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
+    const long long ctas = (long long)p.B * p.H * p.nblk;
+    if (p.seg_len <= 0 || ctas <= 0 || p.T <= 0) return cudaSuccess;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    CUtensorMap tk, tv;
+    if (!make_token_map_full(&tk, p.k, p.T, p.H) || !make_token_map_full(&tv, p.v, p.T, p.H))
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {false};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev]) {
+            e = cudaFuncSetAttribute(block_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    block_state_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -225,22 +225,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int H = p.H;
     const int vb = blockIdx.x % NV;
-    const int bh = blockIdx.x / NV;
+    const int rest = blockIdx.x / NV;
+    const int g = rest % p.nseg;  // segment of the request (0 when not split)
+    const int bh = rest / p.nseg;
     const int h = bh % H;
     const int b = bh / H;
 
     // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
     const int slot = p.state_idx[b];
-    const int t0 = p.cu_seqlens[b];
-    const int t1 = p.cu_seqlens[b + 1];
+    const int t_req0 = p.cu_seqlens[b];
+    const int t_req1 = p.cu_seqlens[b + 1];
     if (slot < 0 || slot >= p.num_slots) {
-        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
         return;
     }
-    if (t0 < 0 || t1 < t0 || t1 > p.T) {
-        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
+    if (t_req0 < 0 || t_req1 < t_req0 || t_req1 > p.T) {
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
         return;
     }
+    // Segment [t0, t1) of the request: the whole request unless long requests are split.
+    const int n_req = t_req1 - t_req0;
+    int nseg_b = 1, t0 = t_req0, t1 = t_req1;
+    if (p.seg_len > 0) {
+        nseg_b = n_req > 0 ? (n_req + p.seg_len - 1) / p.seg_len : 1;
+        if (g >= nseg_b) return;
+        t0 = t_req0 + g * p.seg_len;
+        t1 = min(t_req1, t0 + p.seg_len);
+    }
+    const bool split = nseg_b > 1;
+    const bool last_seg = g == nseg_b - 1;
     const int n = t1 - t0;
     const int nchunks = (n + C - 1) / C;
     const uint64_t limit = p.wait_limit_ns;
@@ -423,7 +436,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *sP = sm + OFF_P;
         {
             float S[32];
-            if (p.prefix_mask[b]) {
+            if (split) {
+                // S = e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, from the
+                // workspace the block-state kernel filled (the pool slot is rewritten by the
+                // request's last segment, so no segment reads it).
+                const float *w0 = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) *
+                                             (kHeadDim * kHeadDim) +
+                                  (size_t)i * kHeadDim + col0;
+                const float d0 = expf(-slope * (float)g * (float)p.seg_len);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 f = reinterpret_cast<const float4 *>(w0)[x];
+                    S[4 * x] = d0 * f.x;
+                    S[4 * x + 1] = d0 * f.y;
+                    S[4 * x + 2] = d0 * f.z;
+                    S[4 * x + 3] = d0 * f.w;
+                }
+                const int nb = g * (p.seg_len / p.blk_len);
+                for (int kb = 0; kb < nb; ++kb) {
+                    const float dk =
+                        expf(-slope * (float)(g * p.seg_len - (kb + 1) * p.blk_len));
+                    const float4 *wk = reinterpret_cast<const float4 *>(
+                        w0 + (size_t)(1 + kb) * (kHeadDim * kHeadDim));
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const float4 f = wk[x];
+                        S[4 * x] = fmaf(dk, f.x, S[4 * x]);
+                        S[4 * x + 1] = fmaf(dk, f.y, S[4 * x + 1]);
+                        S[4 * x + 2] = fmaf(dk, f.z, S[4 * x + 2]);
+                        S[4 * x + 3] = fmaf(dk, f.w, S[4 * x + 3]);
+                    }
+                }
+            } else if (p.prefix_mask[b]) {
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const float4 f = *reinterpret_cast<const float4 *>(gstate + 4 * x);
@@ -593,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Final state write-back (also for zero-length requests).  Skipped after an abort: the
         // error word already reports the failure.
-        if (ok && !*abort_flag) {
+        if (ok && !*abort_flag && last_seg) {
             uint32_t w[32];
             tmem_ld32(t_s, w);
             tmem_ld_wait_regs(w);
@@ -636,8 +680,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // [T][H*128] bf16, box of 64 columns x C rows, 128-byte swizzle; rows past T read as zero.
-bool make_token_map(CUtensorMap *m, const void *ptr, int T, int H) {
+bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)T};
@@ -650,10 +696,8 @@ bool make_token_map(CUtensorMap *m, const void *ptr, int T, int H) {
            CUDA_SUCCESS;
 }
 
-}  // namespace
-
 cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream) {
-    const long long units = (long long)p.B * p.H * NV;
+    const long long units = (long long)p.B * p.H * NV * (p.seg_len > 0 ? p.nseg : 1);
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap tq, tk, tv;
@@ -661,8 +705,8 @@ cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream) {
     memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv));
     if (p.T > 0) {
-        if (!make_token_map(&tq, p.q, p.T, p.H) || !make_token_map(&tk, p.k, p.T, p.H) ||
-            !make_token_map(&tv, p.v, p.T, p.H))
+        if (!make_token_map_full(&tq, p.q, p.T, p.H) || !make_token_map_full(&tk, p.k, p.T, p.H) ||
+            !make_token_map_full(&tv, p.v, p.T, p.H))
             return cudaErrorInvalidValue;
     }
     int dev = 0;

@@ -46,8 +46,26 @@ struct ExtendParams {
     unsigned int *err;
     int B, T, H, num_slots, max_seqlen;
     unsigned long long wait_limit_ns;  // bound on every mbarrier wait
+    // Sequence split of long requests (seg_len == 0: none).  A request of n tokens is cut into
+    // segments of seg_len tokens, processed by separate CTAs; segment g starts from
+    // e^{-s g seg_len} S0 + sum over the blocks k before it of e^{-s (g seg_len - (k+1) blk_len)} B_k,
+    // where B_k is block k's local end state (blk_len tokens, from zero) and S0 the initial state,
+    // both written to the workspace by the block-state kernel beforehand.
+    int seg_len;   // multiple of blk_len
+    int blk_len;   // multiple of the chunk length
+    int nseg;      // segments per request, upper bound over the batch
+    int nblk;      // blocks per request kept in the workspace
+    float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
 };
 
+// Split plan for a batch, from its shape and the device's SM count (seg_len == 0: no split).
+struct SplitPlan {
+    int seg_len, blk_len, nseg, nblk;
+    unsigned long long ws_bytes;
+};
+SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms);
+
 cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);
+cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
 
 }  // namespace la

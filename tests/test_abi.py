@@ -62,20 +62,26 @@ def test_slopes_reject_bad_arguments(lib):
 def test_host_argument_checks_need_no_gpu(lib):
     n = None
     # unsupported head_dim is refused before anything touches the device
-    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 64, 1, n) == 2
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 64, 1, n, 0, n) == 2
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 1, 64, n) == 2
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 1, 1, 64, n) == 2
     # negative sizes / bad counts
-    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, -1, 0, 1, 128, 0, n) == 1
-    assert lib.la_extend(n, n, n, n, n, 0, n, n, n, n, 1, 1, 1, 128, 1, n) == 1
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, -1, 0, 1, 128, 0, n, 0, n) == 1
+    assert lib.la_extend(n, n, n, n, n, 0, n, n, n, n, 1, 1, 1, 128, 1, n, 0, n) == 1
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 0, 128, n) == 1
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 0, 1, 128, n) == 1
     # null pointers with work to do
-    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 128, 1, n) == 1
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 1, 1, 1, 128, 1, n, 0, n) == 1
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 1, 1, 128, n) == 1
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 1, 2, 1, 128, n) == 1
+    import ctypes as ct
+    nb = ct.c_size_t(7)
+    assert lib.la_extend_workspace_size(1, 1, 1, 64, 1, ct.byref(nb)) == 2
+    assert lib.la_extend_workspace_size(-1, 1, 1, 128, 1, ct.byref(nb)) == 1
+    assert lib.la_extend_workspace_size(1, 1, 1, 128, 1, None) == 1
+    assert lib.la_extend_workspace_size(0, 0, 1, 128, 0, ct.byref(nb)) == 0 and nb.value == 0
     # empty batch is a no-op
-    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 0, 0, 1, 128, 0, n) == 0
+    assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 0, 0, 1, 128, 0, n, 0, n) == 0
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 0, 1, 128, n) == 0
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 0, 1, 1, 128, n) == 0
 
