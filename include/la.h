@@ -124,6 +124,30 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
 la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, size_t *bytes);
 
 /*
+ * la_extend_noalloc -- la_extend for callers that cannot allocate device memory.
+ * No counterpart on the paper: this is a convenience of this library.  la_extend may need scratch
+ * memory for long requests in small batches (see la_extend_workspace_size), which the caller must
+ * allocate; a caller that cannot -- a plugin inside a host framework that owns the device's memory
+ * budget and hands over only input and output buffers, or a latency-critical loop that must not
+ * call cudaMalloc -- uses this entry point instead.  It takes la_extend's arguments without the
+ * workspace and computes the same result, using a fixed 16 MiB scratch array that the library
+ * keeps in device memory on every device that loads it (held until the process exits).
+ *   - It allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - A batch whose split plan needs more than 16 MiB of scratch is rejected with
+ *     LA_ERR_UNSUPPORTED before anything is launched (on a 152-SM GB300 every plan fits; use
+ *     la_extend with a workspace otherwise).
+ *   - The first call on a device looks up the array's device address and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's contents; nothing in it
+ *     needs to start at zero, but calls that overlap on the GPU race on it: serialise them.
+ */
+la_status la_extend_noalloc(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                            const float *slopes, float *state_pool, int num_slots,
+                            const int32_t *state_idx, const int32_t *cu_seqlens,
+                            const uint8_t *prefix_mask, la_bf16 *out, int B, int T, int H, int D,
+                            int max_seqlen, la_stream stream);
+
+/*
  * la_decode -- one decode token per request, state updated in place.
  * The recurrence of [LA-page §独立参考实现] for a single token; the page's section
  * "输入与配置覆盖" names the matching decode kernel.  For each request b and head h:

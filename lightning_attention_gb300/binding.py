@@ -180,6 +180,43 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     return out
 
 
+def extend_noalloc(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
+                   max_seqlen: int | None = None):
+    """la_extend_noalloc: la_extend for callers that cannot allocate device memory.  Same result
+    as extend(); any scratch comes from the library's fixed 16 MiB device array instead of a
+    caller buffer, so calls on one device must not overlap on the GPU.  (This wrapper allocates
+    `out` only when the caller does not pass it.)"""
+    lib = load()
+    if not getattr(lib.la_extend_noalloc, "_la_bound", False):
+        vp, ip = ctypes.c_void_p, ctypes.c_int
+        lib.la_extend_noalloc.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip,
+                                          ip, vp]
+        lib.la_extend_noalloc.restype = ip
+        lib.la_extend_noalloc._la_bound = True
+    dev = q.device
+    T = q.shape[0]
+    num_slots, H, D, _ = state_pool.shape
+    B = state_idx.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (T, H * D))
+    _need(slopes_, "slopes", torch.float32, dev, (H,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, (B + 1,))
+    _need(prefix_mask, "prefix_mask", torch.uint8, dev, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (T, H * D))
+    if max_seqlen is None:
+        max_seqlen = T
+    with torch.cuda.device(dev):
+        st = lib.la_extend_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                   num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),
+                                   _ptr(out), B, T, H, D, int(max_seqlen), _stream_handle(dev))
+    _check("la_extend_noalloc", st)
+    return out
+
+
 def decode(q, k, v, slopes_, state_pool, state_idx, out=None):
     """One-token decode (la_decode).  q, k, v: bf16 [B, H*D]; pool updated in place."""
     dev = q.device
