@@ -205,6 +205,7 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     p.nseg = 1;
     p.nblk = 0;
     p.ws = nullptr;
+    p.lpt = (B > 1 && B <= 256) ? 1 : 0;
     if (workspace != nullptr && aligned16(workspace) && T > 0) {
         int sms = 0;
         if ((st = num_sms(&sms)) != LA_OK) return st;

@@ -229,7 +229,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = rest % p.nseg;  // segment of the request (0 when not split)
     const int bh = rest / p.nseg;
     const int h = bh % H;
-    const int b = bh / H;
+    int b = bh / H;
+    if (p.lpt) {
+        // Longest request first: CTAs are issued in index order, so taking requests in
+        // decreasing length order (ties by index) keeps long requests from finishing last.
+        // The b-th CTA group takes the request of rank b; every thread ranks a share of the
+        // requests (B is small when this is on).
+        __shared__ int s_req;
+        const int want = b;
+        for (int t = threadIdx.x; t < p.B; t += kThreads) {
+            const int lt = p.cu_seqlens[t + 1] - p.cu_seqlens[t];
+            int rank = 0;
+            for (int u = 0; u < p.B; ++u) {
+                const int lu = p.cu_seqlens[u + 1] - p.cu_seqlens[u];
+                rank += (lu > lt) || (lu == lt && u < t);
+            }
+            if (rank == want) s_req = t;
+        }
+        __syncthreads();
+        b = s_req;
+    }
 
     // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
     const int slot = p.state_idx[b];

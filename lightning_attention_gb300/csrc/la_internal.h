@@ -56,6 +56,7 @@ struct ExtendParams {
     int nseg;      // segments per request, upper bound over the batch
     int nblk;      // blocks per request kept in the workspace
     float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
+    int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
 };
 
 // Split plan for a batch, from its shape and the device's SM count (seg_len == 0: no split).
