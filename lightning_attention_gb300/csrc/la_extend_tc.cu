@@ -14,10 +14,10 @@
 // exponentials (e^{-s i} / e^{-s j} overflows for s*C large).
 //
 // One CTA owns one (request b, head h, v-column block of DV = 64) and walks the request's chunks
-// of C = 128 tokens in order.  Roles (320 threads):
+// of C = 128 tokens in order.  Roles (384 threads):
 //   warp 8      TMA producer: Q, K (C x 128) and the V block (C x 64) of each chunk into a
-//               two-stage ring (128-byte swizzled tiles, one mbarrier per stage); the whole warp
-//               then converts the landed V tile to fp16 in place, off the epilogue's path;
+//               two-stage ring (128-byte swizzled tiles, one mbarrier per stage);
+//   warps 10-11 convert each landed V tile to fp16 in place, off the epilogue's path;
 //   warp 9      TMEM allocator and MMA issuer (one thread), all accumulating in fp32:
 //                 MMA1  A_c      = Q K^T                      bf16 x bf16  (M=N=K=128)
 //                 MMA2  Oint_c   = Q S_hi + Q S_lo            bf16 x bf16  (M=128, N=64, K=128)
@@ -37,12 +37,14 @@
 // master state S (64), kept in tensor memory rather than registers.
 //
 // Issue order for chunk c: MMA2_c as soon as the previous state is written (s_ready) and the
-// previous outputs have been read (o_free); MMA4_c then MMA3_c once the mask pass (p_ready) and
-// the fp16 V tile (v_ready) are in; then MMA1_{c+1}.  The epilogue handles chunk c as mask,
-// state, out.  Reuse of the other buffers follows from these orders: MMA1_{c+1} overwrites the
-// A buffer of chunk c-1 after p_ready(c); the mask pass of chunk c+1 rewrites P after out(c) has
-// waited for MMA3_c; state(c) rewrites S_hi/S_lo after u_full(c), which by issue order also
-// covers MMA2_c; MMA4_c overwrites U after s_ready(c), i.e. after state(c-1) has read it.
+// previous outputs have been read (o_free); MMA4_c once K is scaled (k_ready) and the fp16 V tile
+// is in (v_ready); MMA3_c once P is written (p_ready); then MMA1_{c+1} into the other A buffer.
+// The epilogue handles chunk c as: scale K, build P, state, out -- so MMA4_c runs while P is
+// built and MMA3_c while the state pass runs.  Reuse of the other buffers follows from these
+// orders: MMA1_{c+2} overwrites the A buffer of chunk c after p_ready(c); the mask pass of chunk
+// c+1 rewrites P after out(c) has waited for MMA3_c; state(c) rewrites S_hi/S_lo after u_full(c),
+// which by issue order also covers MMA2_c; MMA4_c overwrites U after s_ready(c), i.e. after
+// state(c-1) has read it.
 //
 // Every mbarrier wait is bounded (a globaltimer deadline).  A wait that runs out sets the error
 // word and an abort flag; every role then leaves its loop, the producer waits for its own copies
@@ -67,7 +69,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kConvWarp0 = 10;      // warps 10, 11: V tile to fp16
+constexpr int kConvWarps = 2;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_A = 0;        // 2 x 128 columns
 constexpr uint32_t TM_OI = 256;     // DV columns: Q S
@@ -104,7 +108,8 @@ struct Bars {
     uint64_t empty[2];    // MMA -> TMA: stage consumed (MMA3/MMA4 of the chunk done)
     uint64_t a_full[2];   // MMA1 done
     uint64_t v_ready[2];  // producer warp: V tile converted to fp16
-    uint64_t p_ready;     // epilogue: P written, K scaled (8 warp arrivals)
+    uint64_t k_ready;     // epilogue: K scaled by lambda into fp16 (8 warp arrivals)
+    uint64_t p_ready;     // epilogue: P written (8 warp arrivals)
     uint64_t s_ready;     // epilogue: S_hi/S_lo written, U read (8)
     uint64_t o_free;      // epilogue: Oint/Ointra read (8)
     uint64_t u_full;      // MMA4 done (and, by issue order, MMA2 of the same chunk)
@@ -282,8 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
             mbar_init(&bars->a_full[s], 1);
-            mbar_init(&bars->v_ready[s], 1);
+            mbar_init(&bars->v_ready[s], kConvWarps);
         }
+        mbar_init(&bars->k_ready, kEpiWarps);
         mbar_init(&bars->p_ready, kEpiWarps);
         mbar_init(&bars->s_ready, kEpiWarps);
         mbar_init(&bars->o_free, kEpiWarps);
@@ -311,54 +317,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_base = smem_u32(sm);
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer + V to fp16
-        int issued = 0;  // meaningful in lane 0
-        auto issue = [&](int c) -> bool {
-            const int st = c & 1;
-            if (c >= 2 &&
-                !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
-                return false;
-            const int y = t0 + c * C;
-            const int xq = h * kHeadDim;
-            uint8_t *dst = sm + st * SZ_STAGE;
-            mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
-            tma_load_2d(dst, &tq, &bars->full[st], xq, y);
-            tma_load_2d(dst + 16384, &tq, &bars->full[st], xq + 64, y);
-            tma_load_2d(dst + SZ_QK, &tk, &bars->full[st], xq, y);
-            tma_load_2d(dst + SZ_QK + 16384, &tk, &bars->full[st], xq + 64, y);
-            tma_load_2d(dst + 2 * SZ_QK, &tv, &bars->full[st], xq + vb * DV, y);
-            issued = c + 1;
-            return true;
-        };
-        int ok = 1;
-        if (lane == 0 && nchunks > 0) ok = issue(0);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        for (int c = 0; c < nchunks && ok; ++c) {
-            if (lane == 0 && c + 1 < nchunks) ok = issue(c + 1);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const int st = c & 1;
-            if (!(ok = warp_wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
-                break;
-            // the whole 16 KiB V tile, 16-byte chunks, 32 consecutive chunks per instruction
-            uint4 *vt = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + 2 * SZ_QK);
-            for (int m0 = 0; m0 < (int)(SZ_V / 16 / 32); m0 += 8) {
-                uint4 vbuf[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) vbuf[m] = vt[lane + 32 * (m0 + m)];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) vt[lane + 32 * (m0 + m)] = bf16x8_to_f16x8(vbuf[m], 1.f);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->v_ready[st]);
-        }
-        // Copies still in flight must land before the CTA's shared memory goes away.
+        // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1;
+                if (c >= 2 &&
+                    !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                const int y = t0 + c * C;
+                const int xq = h * kHeadDim;
+                uint8_t *dst = sm + st * SZ_STAGE;
+                mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
+                tma_load_2d(dst, &tq, &bars->full[st], xq, y);
+                tma_load_2d(dst + 16384, &tq, &bars->full[st], xq + 64, y);
+                tma_load_2d(dst + SZ_QK, &tk, &bars->full[st], xq, y);
+                tma_load_2d(dst + SZ_QK + 16384, &tk, &bars->full[st], xq + 64, y);
+                tma_load_2d(dst + 2 * SZ_QK, &tv, &bars->full[st], xq + vb * DV, y);
+                issued = c + 1;
+            }
+            // Copies still in flight must land before the CTA's shared memory goes away.
             for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
                 int dummy = 0;
                 wait_bar(&bars->full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
             }
+        }
+    } else if (warp >= kConvWarp0) {
+        // ------------------------------------------------------------------ V tile to fp16
+        // Two warps convert each landed V tile in place (16 KiB, 16-byte chunks, 64 consecutive
+        // chunks per round), well before MMA3 and MMA4 need it.
+        const int cl = (warp - kConvWarp0) * 32 + lane;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1;
+            if (!warp_wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err)) break;
+            uint4 *vt = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + 2 * SZ_QK);
+            constexpr int kRounds = (int)(SZ_V / 16 / (32 * kConvWarps));  // 16
+#pragma unroll
+            for (int m0 = 0; m0 < kRounds; m0 += 8) {
+                uint4 vbuf[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) vbuf[m] = vt[cl + 32 * kConvWarps * (m0 + m)];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    vt[cl + 32 * kConvWarps * (m0 + m)] = bf16x8_to_f16x8(vbuf[m], 1.f);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->v_ready[st]);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
@@ -384,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dA = tbase + TM_A + (uint32_t)st * 128u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(dA, dQ0 + st * stage_step + kofs(kk), dK0 + st * stage_step + kofs(kk), idA, kk > 0);
+                    mma_bf16(dA, dQ0 + st * stage_step + kofs(kk), dK0 + st * stage_step + kofs(kk),
+                             idA, kk > 0);
                 mma_commit(&bars->a_full[st]);
                 return true;
             };
@@ -401,12 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dHi + mnofs(kk), idI, kk > 0);
+                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dHi + mnofs(kk), idI,
+                             kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dLo + mnofs(kk), idI, 1);
-                // U = (lambda K)^T V and Ointra = P V: need the mask pass and the fp16 V tile
-                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err) ||
+                    mma_bf16(tbase + TM_OI, dQ0 + st * stage_step + kofs(kk), dLo + mnofs(kk), idI,
+                             1);
+                // U = (lambda K)^T V as soon as K is scaled and V converted: it runs while the
+                // epilogue builds P
+                if (!wait_bar(&bars->k_ready, c & 1, limit, abort_flag, p.err) ||
                     !wait_bar(&bars->v_ready[st], (c >> 1) & 1, limit, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -414,11 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_U, dKt0 + st * stage_step + mnofs(kk), dV0 + st * stage_step + mnofs(kk), idU, kk > 0);
+                    mma_bf16(tbase + TM_U, dKt0 + st * stage_step + mnofs(kk),
+                             dV0 + st * stage_step + mnofs(kk), idU, kk > 0);
                 mma_commit(&bars->u_full);
+                // Ointra = P V once P is written: it runs while the epilogue does the state pass
+                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_OP, dP + kofs(kk), dV0 + st * stage_step + mnofs(kk), idP, kk > 0);
+                    mma_bf16(tbase + TM_OP, dP + kofs(kk), dV0 + st * stage_step + mnofs(kk), idP,
+                             kk > 0);
                 mma_commit(&bars->o_full);
                 mma_commit(&bars->empty[st]);
                 if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
@@ -525,28 +542,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->a_full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
                 break;
             tc_fence_after();
+            // K row i, 64-column block wg, scaled by lambda_i into fp16 first, so that MMA4 (the
+            // state product) runs while P is built; chunk order rotated by row so that 8
+            // consecutive rows hit 8 distinct banks
+            {
+                const float lam = i < r ? tab[r - 1 - i] : 0.f;
+                uint4 *krow =
+                    reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_QK + wg * 16384 + i * 128);
+#pragma unroll
+                for (int h4 = 0; h4 < 8; h4 += 4) {
+                    uint4 kbuf[4];
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + i) & 7];
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        krow[(h4 + ch + i) & 7] = bf16x8_to_f16x8(kbuf[ch], lam);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->k_ready);
             {
                 uint32_t va[32];
                 const uint32_t ta = tbase + lane_off + TM_A + (uint32_t)st * 128u;
-                if (blk_a) tmem_ld32(ta + (uint32_t)wg * 32u, va);
-                // K row i, 64-column block wg, scaled by lambda_i while the TMEM load flies;
-                // chunk order rotated by row so that 8 consecutive rows hit 8 distinct banks
-                {
-                    const float lam = i < r ? tab[r - 1 - i] : 0.f;
-                    uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_QK +
-                                                            wg * 16384 + i * 128);
-#pragma unroll
-                    for (int h4 = 0; h4 < 8; h4 += 4) {
-                        uint4 kbuf[4];
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + i) & 7];
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            krow[(h4 + ch + i) & 7] = bf16x8_to_f16x8(kbuf[ch], lam);
-                    }
+                if (blk_a) {
+                    tmem_ld32(ta + (uint32_t)wg * 32u, va);
+                    tmem_ld_wait_regs(va);
+                    store_p_block(sP, i, wg, va, tabp);
                 }
-                tmem_ld_wait_regs(va);
-                if (blk_a) store_p_block(sP, i, wg, va, tabp);
                 if (blk_b) {
                     tmem_ld32(ta + (uint32_t)(wg + 2) * 32u, va);
                     tmem_ld_wait_regs(va);
@@ -595,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bars->o_free);
                 // o = gamma D^-0.5 Oint + Ointra for this thread's row, packed to 4 x 16 bytes
                 const float g = tabp[i + 1];
+
                 uint4 ch[4];
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
