@@ -48,12 +48,14 @@ KERNEL_SOURCE = {
     "verify": "la_recurrent.cu",
     "varlen_extend": "la_extend_tc.cu",
     "long_prefill": "la_extend_tc.cu",
+    "verify_tree": "la_recurrent.cu",
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
     "verify": "recurrent_kernel<1>",
     "varlen_extend": "extend_chunked_kernel",
     "long_prefill": "extend_chunked_kernel",
+    "verify_tree": "recurrent_kernel<3>",
 }
 
 
@@ -111,7 +113,9 @@ def algorithmic(w) -> dict:
         byts = 2 * w.B * H * D * D * 4 + 4 * w.B * H * D * 2
         flops = w.B * H * 4 * D * D
         issued = flops
-    elif w.kind == "verify":
+    elif w.kind in ("verify", "tree"):
+        # tree: the same minimum (root state read once, every draft state written once); states a
+        # fork re-reads from the intermediate buffer are not counted
         tokens = w.B * w.N
         byts = w.B * H * D * D * 4 * (1 + w.N) + 4 * w.B * w.N * H * D * 2
         flops = tokens * H * 4 * D * D
@@ -244,7 +248,8 @@ class GpuCase:
         self.idx = w.state_idx.to(dev)
         self.out = torch.empty_like(self.q)
         self.launches_per_step = 1
-        self.kernel = KERNEL_NAME[{"decode": "decode", "verify": "verify"}.get(w.kind, "varlen_extend")]
+        self.kernel = KERNEL_NAME[{"decode": "decode", "verify": "verify",
+                                   "tree": "verify_tree"}.get(w.kind, "varlen_extend")]
         if w.kind == "extend":
             self.cu = w.cu_seqlens.to(dev)
             self.pm = w.prefix_mask.to(dev)
@@ -254,8 +259,10 @@ class GpuCase:
                 # long requests split into segments: block-state kernel, then the extend kernel
                 self.launches_per_step = 2
                 self.kernel = "block_state_kernel + extend_chunked_kernel (one la_extend call)"
-        if w.kind == "verify":
+        if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
+        if w.kind == "tree":
+            self.parents = w.parents.to(dev)
 
     def step(self, q=None, k=None, v=None, idx=None):
         la, w = self.la, self.w
@@ -268,6 +275,9 @@ class GpuCase:
         elif w.kind == "verify":
             la.verify_chain(q, k, v, self.slopes, self.pool, idx, w.N,
                             inter_states=self.inter, out=self.out)
+        elif w.kind == "tree":
+            la.verify_tree(q, k, v, self.slopes, self.pool, idx, self.parents, w.N,
+                           inter_states=self.inter, out=self.out)
         else:
             la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=self.out,
                       max_seqlen=self.max_seqlen)
@@ -380,9 +390,9 @@ def oracle_sample(w, budget_pairs: int):
         B = min(w.B, max(1, budget_pairs // H))
         return {"kind": "decode", "B": B, "tokens": B,
                 "desc": f"{B} of {w.B} requests x {H} heads (1 token each)"}
-    if w.kind == "verify":
+    if w.kind in ("verify", "tree"):
         B = min(w.B, max(1, budget_pairs // (H * w.N)))
-        return {"kind": "verify", "B": B, "tokens": B * w.N,
+        return {"kind": w.kind, "B": B, "tokens": B * w.N,
                 "desc": f"{B} of {w.B} requests x {w.N} draft tokens x {H} heads"}
     lens = (w.cu_seqlens[1:] - w.cu_seqlens[:-1]).numpy()
     # token-heads budget: budget_pairs counts token-heads here
@@ -421,6 +431,15 @@ def run_oracle_sample(w, sample, threads):
         oracle.verify_chain(q, k, v, s, pool, np.arange(B, dtype=np.int32), w.N, w.H, D,
                             nthreads=threads)
         return time.perf_counter() - t0
+    if sample["kind"] == "tree":
+        B = sample["B"]
+        rows = B * w.N
+        q, k, v = (t[:rows].float().numpy().astype(np.float64) for t in (w.q, w.k, w.v))
+        pool = w.prefix_states[:B].double().numpy()
+        t0 = time.perf_counter()
+        oracle.verify_tree(q, k, v, s, pool, np.arange(B, dtype=np.int32), w.parents[:B].numpy(),
+                           w.N, w.H, D)
+        return time.perf_counter() - t0
     if sample["kind"] == "extend_prefix":
         n = sample["n"]
         q, k, v = (t[:n].float().numpy().astype(np.float64) for t in (w.q, w.k, w.v))
@@ -443,7 +462,8 @@ def run_oracle_sample(w, sample, threads):
 
 
 ORACLE_BUDGET = {  # (request, head) pairs or token-heads per sample: ~1-10 s of fp64 CPU work
-    "decode": 4096, "verify": 64 * 5 * 16, "varlen_extend": 16 * 2400, "long_prefill": 32 * 1200}
+    "decode": 4096, "verify": 64 * 5 * 16, "varlen_extend": 16 * 2400, "long_prefill": 32 * 1200,
+    "verify_tree": 64 * 8 * 8}
 
 
 def cpu_baseline(name, w, threads):
@@ -471,8 +491,10 @@ def workload_config(name, w, world):
            "requests_per_gpu": w.B, "tokens_per_gpu_step": algorithmic(w)["tokens"],
            "parallelism": f"replicas{world}" if world > 1 else "single_gpu",
            "l2": "inputs larger than L2 (129 MB); no flush"}
-    if w.kind == "verify":
+    if w.kind in ("verify", "tree"):
         cfg["draft_tokens"] = w.N
+    if w.kind == "tree":
+        cfg["tree_parents"] = [int(x) for x in w.parents[0]]
     if w.kind == "decode":
         cfg["pool_slots"] = w.num_slots
     return cfg

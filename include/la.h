@@ -185,10 +185,28 @@ la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
                           int N, int H, int D, la_stream stream);
 
 /*
+ * la_verify_tree -- tree target verify (EAGLE-style, topk > 1) of N draft tokens per request.
+ * [LA-page §生产环境不支持, item 3 and §Next Work, item 2]: the page's seg_la handles draft tokens
+ * only as a chain and names the kernel-level fix -- each draft token forks from the state saved
+ * for its parent.  This call is that fix: for each request b and head h, draft token t continues
+ * from the state after token parents[b*N + t] (from state_pool[state_idx[b], h] when that is -1),
+ * its output row is written and its state stored into inter_states[b][t][h].  A chain
+ * (parents[t] = t - 1) gives exactly la_verify_chain's results.  The pool is only read.
+ *   parents       device, int32 [B][N]; each entry in [-1, t-1] (topologically ordered tree)
+ *   other arguments as for la_verify_chain
+ * A request with a parent outside [-1, t-1] is skipped (nothing written) and la_poll_error
+ * reports LA_ERR_DEVICE_INPUT.
+ */
+la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                         const float *slopes, const float *state_pool, int num_slots,
+                         const int32_t *state_idx, const int32_t *parents, float *inter_states,
+                         la_bf16 *out, int B, int N, int H, int D, la_stream stream);
+
+/*
  * la_poll_error -- synchronise `stream`, then read and clear the current device's error word.
  * Returns LA_ERR_TIMEOUT if a bounded device wait ran out, LA_ERR_DEVICE_INPUT if a kernel found
- * a slot index out of range or inconsistent cu_seqlens, LA_ERR_CUDA if the stream reports a CUDA
- * error, else LA_OK.  This is the one call that blocks the host.
+ * a slot index out of range, inconsistent cu_seqlens or a tree parent out of range, LA_ERR_CUDA if
+ * the stream reports a CUDA error, else LA_OK.  This is the one call that blocks the host.
  */
 la_status la_poll_error(la_stream stream);
 

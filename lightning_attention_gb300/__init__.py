@@ -5,4 +5,4 @@ include/la.h; this package holds the ctypes binding (binding.py), the in-tree bu
 and the seeded synthetic workloads (workloads.py).
 """
 from .binding import (LAError, decode, extend, extend_noalloc, extend_workspace_size, load,  # noqa
-                      poll_error, set_wait_limit, slopes, verify_chain)
+                      poll_error, set_wait_limit, slopes, verify_chain, verify_tree)

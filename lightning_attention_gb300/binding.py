@@ -24,7 +24,7 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_C
           4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
 
 EXPORTS = ("la_slopes", "la_extend", "la_extend_workspace_size", "la_decode", "la_verify_chain",
-           "la_poll_error", "la_status_string", "la_set_wait_limit")
+           "la_verify_tree", "la_poll_error", "la_status_string", "la_set_wait_limit")
 
 
 class LAError(RuntimeError):
@@ -63,6 +63,8 @@ def load():
         lib.la_decode.restype = ip
         lib.la_verify_chain.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, ip, ip, ip, ip, vp]
         lib.la_verify_chain.restype = ip
+        lib.la_verify_tree.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, vp]
+        lib.la_verify_tree.restype = ip
         lib.la_poll_error.argtypes = [vp]
         lib.la_poll_error.restype = ip
         lib.la_status_string.argtypes = [ip]
@@ -259,4 +261,31 @@ def verify_chain(q, k, v, slopes_, state_pool, state_idx, N: int, inter_states=N
                                     num_slots, _ptr(state_idx), _ptr(inter_states), _ptr(out), B,
                                     N, H, D, _stream_handle(dev))
     _check("la_verify_chain", st)
+    return out, inter_states
+
+
+def verify_tree(q, k, v, slopes_, state_pool, state_idx, parents, N: int, inter_states=None,
+                out=None):
+    """Tree verify (la_verify_tree).  parents: int32 [B, N] with entries in [-1, t-1] (-1: the
+    pool state).  q, k, v: bf16 [B*N, H*D]; returns (out, inter_states); the pool is not modified."""
+    dev = q.device
+    num_slots, H, D, _ = state_pool.shape
+    B = state_idx.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (B * N, H * D))
+    _need(slopes_, "slopes", torch.float32, dev, (H,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    _need(parents, "parents", torch.int32, dev, (B, N))
+    if inter_states is None:
+        inter_states = torch.empty((B, N, H, D, D), dtype=torch.float32, device=dev)
+    _need(inter_states, "inter_states", torch.float32, dev, (B, N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (B * N, H * D))
+    with torch.cuda.device(dev):
+        st = load().la_verify_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                   num_slots, _ptr(state_idx), _ptr(parents), _ptr(inter_states),
+                                   _ptr(out), B, N, H, D, _stream_handle(dev))
+    _check("la_verify_tree", st)
     return out, inter_states

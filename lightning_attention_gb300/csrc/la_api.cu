@@ -108,7 +108,8 @@ la_status la_poll_error(la_stream stream) {
             return LA_ERR_CUDA;
     }
     if (word & la::ERR_BIT_TIMEOUT) return LA_ERR_TIMEOUT;
-    if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS)) return LA_ERR_DEVICE_INPUT;
+    if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS | la::ERR_BIT_PARENTS))
+        return LA_ERR_DEVICE_INPUT;
     return LA_OK;
 }
 
@@ -164,6 +165,36 @@ la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     la_status st = error_word_ptr(&p.err);
     if (st != LA_OK) return st;
     return launch_status(la::launch_recurrent(la::RECUR_VERIFY, p, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                         const float *slopes, const float *state_pool, int num_slots,
+                         const int32_t *state_idx, const int32_t *parents, float *inter_states,
+                         la_bf16 *out, int B, int N, int H, int D, la_stream stream) {
+    if (B < 0 || N < 1 || H < 1 || D < 1 || num_slots < 1) return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * N > 0x7fffffffLL) return LA_ERR_INVALID;
+    if (B == 0) return LA_OK;
+    if (!q || !k || !v || !slopes || !state_pool || !state_idx || !parents || !inter_states || !out)
+        return LA_ERR_INVALID;
+    la::RecurParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.slopes = slopes;
+    p.pool = const_cast<float *>(state_pool);  // read only in tree mode
+    p.state_idx = state_idx;
+    p.parents = parents;
+    p.inter = inter_states;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.T = B * N;
+    p.num_slots = num_slots;
+    la_status st = error_word_ptr(&p.err);
+    if (st != LA_OK) return st;
+    return launch_status(la::launch_recurrent(la::RECUR_TREE, p, static_cast<cudaStream_t>(stream)));
 }
 
 la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,

@@ -12,12 +12,13 @@ enum : unsigned int {
     ERR_BIT_TIMEOUT = 1u,       // a bounded device wait ran out
     ERR_BIT_SLOT_RANGE = 2u,    // state_idx entry outside [0, num_slots)
     ERR_BIT_SEQLENS = 4u,       // cu_seqlens decreasing or past T
+    ERR_BIT_PARENTS = 8u,       // tree-verify parent index outside [-1, t-1]
 };
 
 constexpr int kHeadDim = 128;
 
 // Recurrent (token-serial) kernels: decode, chain verify, and short extends.
-enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2 };
+enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2, RECUR_TREE = 3 };
 
 struct RecurParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -27,6 +28,7 @@ struct RecurParams {
     const int32_t *cu_seqlens;   // [B+1] (extend)
     const uint8_t *prefix_mask;  // [B]   (extend)
     float *inter;                // [B][N][H][D][D] (verify)
+    const int32_t *parents;      // [B][N] (tree verify)
     __nv_bfloat16 *out;
     unsigned int *err;           // device error word
     int B, H, N, T, num_slots;

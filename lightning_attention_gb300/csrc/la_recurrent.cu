@@ -3,7 +3,8 @@
 // Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
 // "独立参考实现：逐 token 递推公式":  S_t = S_{t-1} * exp(-slope_h) + outer(k_t, v_t),
 // o_t = (q_t @ S_t) * D^-0.5.  Chain verify follows the same page's section "生产环境不支持",
-// item 3 (every draft token continues from the previous position).
+// item 3 (every draft token continues from the previous position); tree verify follows its
+// section "Next Work", item 2 (each draft token forks from the state saved for its parent).
 //
 // These paths are HBM-bound: per (request, head) the 128 x 128 fp32 state (64 KiB) is read once,
 // updated token by token in registers, and written once (decode: back to the pool; verify: once
@@ -73,6 +74,18 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
         t_begin = b * p.N;
         n = p.N;
     }
+    if (MODE == RECUR_TREE) {
+        // parents must point backwards; checked up front so that a bad tree writes nothing
+        bool bad = false;
+        for (int t = 0; t < n; ++t) {
+            const int par = p.parents[(size_t)b * p.N + t];
+            bad |= par < -1 || par >= t;
+        }
+        if (bad) {
+            if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_PARENTS);
+            return;
+        }
+    }
 
     float4 s[kRowsPerWarp];
     if (from_pool) {
@@ -89,6 +102,22 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
     const size_t row_stride = (size_t)H * kHeadDim;
 
     for (int t = 0; t < n; ++t) {
+        if (MODE == RECUR_TREE) {
+            // Fork: unless the parent is the previous token (state already in registers), reload
+            // the parent's state -- the pool slot for the root, else the intermediate state this
+            // thread itself stored for the parent (same elements, so no cross-thread ordering).
+            const int par = p.parents[(size_t)b * p.N + t];
+            if (par != t - 1) {
+                const float *src =
+                    par < 0 ? state
+                            : p.inter + (((size_t)b * p.N + par) * H + h) *
+                                            (size_t)(kHeadDim * kHeadDim);
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    s[r] = *reinterpret_cast<const float4 *>(src + (size_t)(row0 + r) * kHeadDim +
+                                                             col);
+            }
+        }
         const size_t tok = (size_t)(t_begin + t) * row_stride + (size_t)h * kHeadDim;
         // this warp's 16 k and q entries (same address across the warp: a broadcast) and this
         // lane's 4 v entries
@@ -115,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
             o.z = fmaf(qf[r], s[r].z, o.z);
             o.w = fmaf(qf[r], s[r].w, o.w);
         }
-        if (MODE == RECUR_VERIFY) {
+        if (MODE == RECUR_VERIFY || MODE == RECUR_TREE) {
             float *dst = p.inter + (((size_t)b * p.N + t) * H + h) * (size_t)(kHeadDim * kHeadDim);
 #pragma unroll
             for (int r = 0; r < kRowsPerWarp; ++r)
@@ -139,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
         // token t + 1, so one barrier per token is enough.
     }
 
-    if (MODE != RECUR_VERIFY) {
+    if (MODE != RECUR_VERIFY && MODE != RECUR_TREE) {
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r)
             __stcs(reinterpret_cast<float4 *>(state + (size_t)(row0 + r) * kHeadDim + col), s[r]);
@@ -157,6 +186,7 @@ cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t 
         case RECUR_DECODE: recurrent_kernel<RECUR_DECODE><<<grid, block, 0, stream>>>(p); break;
         case RECUR_VERIFY: recurrent_kernel<RECUR_VERIFY><<<grid, block, 0, stream>>>(p); break;
         case RECUR_EXTEND: recurrent_kernel<RECUR_EXTEND><<<grid, block, 0, stream>>>(p); break;
+        case RECUR_TREE: recurrent_kernel<RECUR_TREE><<<grid, block, 0, stream>>>(p); break;
     }
     return cudaGetLastError();
 }

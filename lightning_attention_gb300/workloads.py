@@ -29,7 +29,7 @@ SENTINEL = 54321.0
 @dataclass
 class Workload:
     name: str
-    kind: str                      # "extend", "decode" or "verify"
+    kind: str                      # "extend", "decode", "verify" or "tree"
     H: int
     D: int
     layer_id: int
@@ -46,6 +46,7 @@ class Workload:
     random_pool: bool = False      # decode workload: every slot random
     pool_fill: torch.Tensor | None = None    # fp32 [num_slots, H, D, D] when random_pool
     decode_steps: list = field(default_factory=list)  # tiny workload: [(q, k, v)] per step
+    parents: torch.Tensor | None = None      # int32 [B, N] (tree verify)
 
     @property
     def B(self) -> int:
@@ -164,6 +165,23 @@ def verify_chain(seed: int = 0, B: int = 128, N: int = 5, H: int = 64,
                     prefix_mask=torch.ones(B, dtype=torch.uint8), prefix_states=prefix, N=N)
 
 
+# A binary draft tree of 8 tokens (two children per node, depth 4): token t forks from the state
+# after token EAGLE_TREE8[t]; -1 is the verified prefix (the pool state).
+EAGLE_TREE8 = (-1, 0, 0, 1, 1, 2, 2, 3)
+
+
+def verify_tree(seed: int = 0, B: int = 128, H: int = 64, parents=EAGLE_TREE8,
+                num_slots: int = 512) -> Workload:
+    """Tree target verify (topk > 1): 128 requests x an 8-token draft tree, H=64, layer 10 of L=20;
+    every request has a prefix state in a random slot of a 512-slot pool; all requests share one
+    tree shape.  Same draw order as the chain-verify workload."""
+    w = verify_chain(seed, B=B, N=len(parents), H=H, num_slots=num_slots)
+    w.name = f"verify_tree_b{B}_n{len(parents)}_h{H}"
+    w.kind = "tree"
+    w.parents = torch.tensor([list(parents)] * B, dtype=torch.int32)
+    return w
+
+
 def custom_extend(lengths, H: int = 2, D: int = HEAD_DIM, layer_id: int = 0, L: int = 1,
                   prefix=None, num_slots: int | None = None, seed: int = 0,
                   shuffle_slots: bool = True) -> Workload:
@@ -210,4 +228,5 @@ WORKLOADS = {
     "varlen_extend": varlen_extend,
     "long_prefill": long_prefill,
     "verify": verify_chain,
+    "verify_tree": verify_tree,
 }

@@ -55,6 +55,8 @@ def _bind(lib):
     lib.la_oracle_decode.restype = ci
     lib.la_oracle_verify_chain.argtypes = [dp, dp, dp, dp, dp, ip, dp, dp, ci, ci, ci, ci, ci]
     lib.la_oracle_verify_chain.restype = ci
+    lib.la_oracle_verify_tree.argtypes = [dp, dp, dp, dp, dp, ip, ip, dp, dp, ci, ci, ci, ci]
+    lib.la_oracle_verify_tree.restype = ci
     return lib
 
 
@@ -154,4 +156,27 @@ def verify_chain(q, k, v, slopes_, pool, state_idx, N: int, H: int, D: int,
                                    _ptr(pool_c, ctypes.c_double), _ptr(idx, ctypes.c_int32),
                                    _ptr(inter, ctypes.c_double), _ptr(out, ctypes.c_double),
                                    B, N, H, D, nthreads or default_threads())
+    return out, inter
+
+
+def verify_tree(q, k, v, slopes_, pool, state_idx, parents, N: int, H: int, D: int, lib=None):
+    """Tree verify: token t of request b continues from the state after token parents[b, t] (-1:
+    the pool state).  q, k, v: [B*N, H*D]; parents: [B, N] int32.  Returns (out, inter) like
+    verify_chain; raises ValueError if a parent does not point backwards."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    s = _f64(slopes_)
+    pool_c = _f64(pool)
+    idx = _i32(state_idx)
+    par = _i32(parents)
+    B = idx.shape[0]
+    assert q.shape == (B * N, H * D) and par.shape == (B, N)
+    out = np.zeros((B * N, H * D), dtype=np.float64)
+    inter = np.zeros((B, N, H, D, D), dtype=np.float64)
+    rc = (lib or _load()).la_oracle_verify_tree(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+        _ptr(s, ctypes.c_double), _ptr(pool_c, ctypes.c_double), _ptr(idx, ctypes.c_int32),
+        _ptr(par, ctypes.c_int32), _ptr(inter, ctypes.c_double), _ptr(out, ctypes.c_double),
+        B, N, H, D)
+    if rc != 0:
+        raise ValueError("parents must satisfy -1 <= parents[b, t] < t")
     return out, inter

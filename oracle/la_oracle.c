@@ -16,6 +16,8 @@
  *       slopes * (1 - layer_id/(L-1) + 1e-5), and slopes * (1 + 1e-5) when L = 1.
  *   [LA-page §生产环境不支持 item 3]  chain (topk = 1) target verify: every draft token continues
  *       from the previous position's state.
+ *   [LA-page §Next Work, item 2]  tree verify: each draft token forks from the state saved for
+ *       its parent, not from the previous position of the chain.
  *
  * Everything is evaluated in double precision straight from those definitions: no chunking, no
  * blocking, no reassociation.  The state is S[i][j] with i on the k index (rows) and j on the v
@@ -26,7 +28,9 @@
  *   - decay is applied before the outer product is added, so the current token has weight 1;
  *   - a request whose prefix flag is 0 starts from the zero state and never reads its slot;
  *   - the final state is written back for every request, including zero-length ones;
- *   - chain verify leaves the pool untouched and records the state after each draft token.
+ *   - chain verify leaves the pool untouched and records the state after each draft token;
+ *   - tree verify: parent[t] in [-1, t-1], -1 meaning the request's pool state; the state after
+ *     token t is the recurrence applied to token t from the state after its parent.
  *
  * Threads: the (request, head) pairs are independent, so they are spread over POSIX threads.
  * This changes no arithmetic: every pair is still one plain sequential loop.
@@ -194,6 +198,45 @@ int la_oracle_decode(const double *q, const double *k, const double *v, const do
     a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool; a.state_idx = state_idx;
     a.out = out; a.B = B; a.H = H; a.D = D; a.nthreads = nthreads;
     return run(&a);
+}
+
+/* Tree verify: like chain verify, but draft token t of request b continues from the state after
+ * token parents[b*N + t] (or from the pool state when that is -1); parents must point backwards.
+ * Returns -1 (and computes nothing) if some parent is out of [-1, t-1]. */
+int la_oracle_verify_tree(const double *q, const double *k, const double *v, const double *slopes,
+                          const double *pool, const int32_t *state_idx, const int32_t *parents,
+                          double *inter, double *out, int B, int N, int H, int D)
+{
+    for (int b = 0; b < B; b++)
+        for (int t = 0; t < N; t++)
+            if (parents[(size_t)b * N + t] < -1 || parents[(size_t)b * N + t] >= t)
+                return -1;
+    const size_t row = (size_t)H * D, dd = (size_t)D * D;
+    const double scale = 1.0 / sqrt((double)D);
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < H; h++) {
+            const double decay = exp(-slopes[h]);
+            const double *root = pool + ((size_t)state_idx[b] * H + h) * dd;
+            for (int t = 0; t < N; t++) {
+                const int par = parents[(size_t)b * N + t];
+                const double *base =
+                    par < 0 ? root : inter + (((size_t)b * N + par) * H + h) * dd;
+                double *S = inter + (((size_t)b * N + t) * H + h) * dd;
+                const size_t off = ((size_t)b * N + t) * row + (size_t)h * D;
+                const double *qt = q + off, *kt = k + off, *vt = v + off;
+                for (int i = 0; i < D; i++)
+                    for (int j = 0; j < D; j++)
+                        S[(size_t)i * D + j] = base[(size_t)i * D + j] * decay + kt[i] * vt[j];
+                for (int j = 0; j < D; j++) {
+                    double acc = 0.0;
+                    for (int i = 0; i < D; i++)
+                        acc += qt[i] * S[(size_t)i * D + j];
+                    out[off + j] = acc * scale;
+                }
+            }
+        }
+    }
+    return 0;
 }
 
 /* Chain verify: q, k, v, out are [B*N][H*D] (request-major, N draft tokens each); the pool is

@@ -49,6 +49,10 @@ MUTANTS = {
                           "        const size_t off = (size_t)b * row + (size_t)h * D;"),
     "request_length_short": ("n = a->cu_seqlens[b + 1] - t0;", "n = a->cu_seqlens[b + 1] - t0 - 1;"),
     "wrong_head_slope": ("recur(S, D, a->slopes[h], n,", "recur(S, D, a->slopes[0], n,"),
+    "tree_forks_from_previous": ("par < 0 ? root : inter + (((size_t)b * N + par) * H + h) * dd;",
+                                 "(t == 0) ? root : inter + (((size_t)b * N + t - 1) * H + h) * dd;"),
+    "tree_forks_from_root": ("par < 0 ? root : inter + (((size_t)b * N + par) * H + h) * dd;",
+                             "root;"),
 }
 
 

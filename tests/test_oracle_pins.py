@@ -237,3 +237,69 @@ def test_thread_count_does_not_change_results():
     o8, p8 = oracle.extend(*args, nthreads=8)
     np.testing.assert_array_equal(o1, o8)
     np.testing.assert_array_equal(p1, p8)
+
+
+def test_tree_verify_chain_shaped_tree_is_chain_verify():
+    H, D, B, N = 2, 8, 3, 5
+    q, k, v = rng_inputs(23, B * N, H, D)
+    slopes = np.array([0.4, 0.03])
+    pool = np.random.default_rng(24).standard_normal((4, H, D, D)) * 0.05
+    idx = np.array([1, 3, 0], dtype=np.int32)
+    chain = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    o_t, i_t = oracle.verify_tree(q, k, v, slopes, pool, idx, chain, N, H, D)
+    o_c, i_c = oracle.verify_chain(q, k, v, slopes, pool, idx, N, H, D)
+    np.testing.assert_array_equal(o_t, o_c)
+    np.testing.assert_array_equal(i_t, i_c)
+
+
+def test_tree_verify_star_is_independent_decodes():
+    """Every parent the root: each draft token is one decode step from the pool state."""
+    H, D, B, N = 2, 8, 2, 4
+    q, k, v = rng_inputs(25, B * N, H, D)
+    slopes = np.array([0.2, 0.7])
+    pool = np.random.default_rng(26).standard_normal((3, H, D, D)) * 0.05
+    idx = np.array([2, 0], dtype=np.int32)
+    star = np.full((B, N), -1, dtype=np.int32)
+    out, inter = oracle.verify_tree(q, k, v, slopes, pool, idx, star, N, H, D)
+    for b in range(B):
+        for t in range(N):
+            row = b * N + t
+            for h in range(H):
+                sl = slice(h * D, (h + 1) * D)
+                S1 = math.exp(-slopes[h]) * pool[idx[b], h] + np.outer(k[row, sl], v[row, sl])
+                np.testing.assert_allclose(inter[b, t, h], S1, rtol=1e-14, atol=1e-16)
+                np.testing.assert_allclose(out[row, sl], q[row, sl] @ S1 / math.sqrt(D),
+                                           rtol=1e-12, atol=1e-14)
+
+
+def test_tree_verify_equals_extend_along_root_paths():
+    """Any tree: token t's state and output equal an extend over the tokens on its root path."""
+    H, D, B, N = 2, 8, 2, 7
+    q, k, v = rng_inputs(27, B * N, H, D)
+    slopes = np.array([0.15, 0.05])
+    pool = np.random.default_rng(28).standard_normal((3, H, D, D)) * 0.05
+    idx = np.array([2, 1], dtype=np.int32)
+    parents = np.array([[-1, 0, 0, 1, -1, 4, 2], [-1, -1, 1, 2, 2, 0, 5]], dtype=np.int32)
+    out, inter = oracle.verify_tree(q, k, v, slopes, pool, idx, parents, N, H, D)
+    for b in range(B):
+        for t in range(N):
+            path, x = [], t
+            while x >= 0:
+                path.append(b * N + x)
+                x = parents[b, x]
+            path = path[::-1]
+            e_out, e_pool = oracle.extend(q[path], k[path], v[path], slopes, pool, [idx[b]],
+                                          [0, len(path)], [1], H, D)
+            np.testing.assert_allclose(inter[b, t], e_pool[idx[b]], rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(out[b * N + t], e_out[-1], rtol=1e-13, atol=1e-15)
+
+
+def test_tree_verify_rejects_forward_parents():
+    H, D = 1, 4
+    q = np.zeros((3, H * D))
+    with pytest.raises(ValueError):
+        oracle.verify_tree(q, q, q, [0.1], np.zeros((1, H, D, D)), [0],
+                           np.array([[-1, 2, 0]], dtype=np.int32), 3, H, D)
+    with pytest.raises(ValueError):
+        oracle.verify_tree(q, q, q, [0.1], np.zeros((1, H, D, D)), [0],
+                           np.array([[-2, 0, 1]], dtype=np.int32), 3, H, D)
