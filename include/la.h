@@ -203,10 +203,29 @@ la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
                          la_bf16 *out, int B, int N, int H, int D, la_stream stream);
 
 /*
+ * la_commit_accepted -- after a verify call, move the state of the last accepted draft token of
+ * each request into its pool slot: state_pool[state_idx[b], h] = inter_states[b][accept_idx[b]][h]
+ * for every head, when accept_idx[b] >= 0 (-1: nothing accepted, the slot is left as is).  With
+ * chain verify accept_idx[b] is (number of accepted tokens - 1); with tree verify it is the last
+ * node of the accepted path.  The verify calls leave the pool alone ([LA-page §生产环境不支持,
+ * item 3]: the page's intermediate-state pipeline is per request); this is the commit step that
+ * completes them.
+ *   inter_states  device, fp32 [B][N][H][D][D] (as written by la_verify_chain / la_verify_tree)
+ *   accept_idx    device, int32 [B], each in [-1, N-1]
+ *   state_pool    device, fp32 [num_slots][H][D][D], updated in place (named slots only)
+ *   state_idx     device, int32 [B]
+ * An index outside [-1, N-1] or a slot out of range skips that request and is reported by
+ * la_poll_error as LA_ERR_DEVICE_INPUT.
+ */
+la_status la_commit_accepted(const float *inter_states, const int32_t *accept_idx,
+                             float *state_pool, int num_slots, const int32_t *state_idx, int B,
+                             int N, int H, int D, la_stream stream);
+
+/*
  * la_poll_error -- synchronise `stream`, then read and clear the current device's error word.
  * Returns LA_ERR_TIMEOUT if a bounded device wait ran out, LA_ERR_DEVICE_INPUT if a kernel found
- * a slot index out of range, inconsistent cu_seqlens or a tree parent out of range, LA_ERR_CUDA if
- * the stream reports a CUDA error, else LA_OK.  This is the one call that blocks the host.
+ * a slot index out of range, inconsistent cu_seqlens, a tree parent or commit index out of range,
+ * LA_ERR_CUDA if the stream reports a CUDA error, else LA_OK.  This is the one call that blocks the host.
  */
 la_status la_poll_error(la_stream stream);
 

@@ -24,7 +24,8 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_C
           4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
 
 EXPORTS = ("la_slopes", "la_extend", "la_extend_workspace_size", "la_decode", "la_verify_chain",
-           "la_verify_tree", "la_poll_error", "la_status_string", "la_set_wait_limit")
+           "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
+           "la_set_wait_limit")
 
 
 class LAError(RuntimeError):
@@ -65,6 +66,8 @@ def load():
         lib.la_verify_chain.restype = ip
         lib.la_verify_tree.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, vp]
         lib.la_verify_tree.restype = ip
+        lib.la_commit_accepted.argtypes = [vp, vp, vp, ip, vp, ip, ip, ip, ip, vp]
+        lib.la_commit_accepted.restype = ip
         lib.la_poll_error.argtypes = [vp]
         lib.la_poll_error.restype = ip
         lib.la_status_string.argtypes = [ip]
@@ -289,3 +292,19 @@ def verify_tree(q, k, v, slopes_, state_pool, state_idx, parents, N: int, inter_
                                    _ptr(out), B, N, H, D, _stream_handle(dev))
     _check("la_verify_tree", st)
     return out, inter_states
+
+
+def commit_accepted(inter_states, accept_idx, state_pool, state_idx):
+    """la_commit_accepted: pool[state_idx[b]] = inter_states[b, accept_idx[b]] where accept_idx[b]
+    >= 0 (-1 leaves the slot as is)."""
+    dev = state_pool.device
+    num_slots, H, D, _ = state_pool.shape
+    B, N = inter_states.shape[0], inter_states.shape[1]
+    _need(inter_states, "inter_states", torch.float32, dev, (B, N, H, D, D))
+    _need(accept_idx, "accept_idx", torch.int32, dev, (B,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    with torch.cuda.device(dev):
+        st = load().la_commit_accepted(_ptr(inter_states), _ptr(accept_idx), _ptr(state_pool),
+                                       num_slots, _ptr(state_idx), B, N, H, D, _stream_handle(dev))
+    _check("la_commit_accepted", st)

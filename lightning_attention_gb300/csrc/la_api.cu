@@ -108,7 +108,8 @@ la_status la_poll_error(la_stream stream) {
             return LA_ERR_CUDA;
     }
     if (word & la::ERR_BIT_TIMEOUT) return LA_ERR_TIMEOUT;
-    if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS | la::ERR_BIT_PARENTS))
+    if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS | la::ERR_BIT_PARENTS |
+                la::ERR_BIT_ACCEPT))
         return LA_ERR_DEVICE_INPUT;
     return LA_OK;
 }
@@ -195,6 +196,28 @@ la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     la_status st = error_word_ptr(&p.err);
     if (st != LA_OK) return st;
     return launch_status(la::launch_recurrent(la::RECUR_TREE, p, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_commit_accepted(const float *inter_states, const int32_t *accept_idx,
+                             float *state_pool, int num_slots, const int32_t *state_idx, int B,
+                             int N, int H, int D, la_stream stream) {
+    if (B < 0 || N < 1 || H < 1 || D < 1 || num_slots < 1) return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (B == 0) return LA_OK;
+    if (!inter_states || !accept_idx || !state_pool || !state_idx) return LA_ERR_INVALID;
+    if (!aligned16(inter_states) || !aligned16(state_pool)) return LA_ERR_INVALID;
+    la::CommitParams p{};
+    p.inter = inter_states;
+    p.accept_idx = accept_idx;
+    p.pool = state_pool;
+    p.state_idx = state_idx;
+    p.B = B;
+    p.N = N;
+    p.H = H;
+    p.num_slots = num_slots;
+    la_status st = error_word_ptr(&p.err);
+    if (st != LA_OK) return st;
+    return launch_status(la::launch_commit(p, static_cast<cudaStream_t>(stream)));
 }
 
 la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,

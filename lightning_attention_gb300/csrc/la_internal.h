@@ -13,6 +13,7 @@ enum : unsigned int {
     ERR_BIT_SLOT_RANGE = 2u,    // state_idx entry outside [0, num_slots)
     ERR_BIT_SEQLENS = 4u,       // cu_seqlens decreasing or past T
     ERR_BIT_PARENTS = 8u,       // tree-verify parent index outside [-1, t-1]
+    ERR_BIT_ACCEPT = 16u,       // commit index outside [-1, N-1]
 };
 
 constexpr int kHeadDim = 128;
@@ -35,6 +36,18 @@ struct RecurParams {
 };
 
 cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream);
+
+// Accepted-state commit: pool[state_idx[b]] = inter[b][accept_idx[b]] (all heads) when
+// accept_idx[b] >= 0.
+struct CommitParams {
+    const float *inter;          // [B][N][H][D][D]
+    const int32_t *accept_idx;   // [B]
+    float *pool;
+    const int32_t *state_idx;
+    unsigned int *err;
+    int B, N, H, num_slots;
+};
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream);
 
 // Chunked tensor-core extend (tcgen05 + TMA).
 struct ExtendParams {

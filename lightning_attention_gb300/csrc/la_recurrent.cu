@@ -175,7 +175,42 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
     }
 }
 
+// One CTA of 256 threads per (request, head): a 64 KiB fp32 copy with 16-byte accesses.
+__global__ void __launch_bounds__(kThreads) commit_kernel(const CommitParams p) {
+    const int b = blockIdx.x / p.H;
+    const int h = blockIdx.x - b * p.H;
+    const int slot = p.state_idx[b];
+    const int a = p.accept_idx[b];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        return;
+    }
+    if (a < -1 || a >= p.N) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_ACCEPT);
+        return;
+    }
+    if (a < 0) return;  // nothing accepted: the slot keeps its state
+    const float4 *src = reinterpret_cast<const float4 *>(
+        p.inter + (((size_t)b * p.N + a) * p.H + h) * (size_t)(kHeadDim * kHeadDim));
+    float4 *dst =
+        reinterpret_cast<float4 *>(p.pool + ((size_t)slot * p.H + h) * (size_t)(kHeadDim * kHeadDim));
+    constexpr int kVec = kHeadDim * kHeadDim / 4;
+    float4 buf[kVec / kThreads];
+#pragma unroll
+    for (int x = 0; x < kVec / kThreads; ++x) buf[x] = __ldcs(src + threadIdx.x + x * kThreads);
+#pragma unroll
+    for (int x = 0; x < kVec / kThreads; ++x) dst[threadIdx.x + x * kThreads] = buf[x];
+}
+
 }  // namespace
+
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream) {
+    const long long blocks = (long long)p.B * p.H;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    commit_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.H;

@@ -8,7 +8,7 @@ generator, which holds none of the method's arithmetic.
 The arithmetic lives in ``la_oracle.c`` (plain C, double precision), written from the page
 "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
 "独立参考实现：逐 token 递推公式" (independent reference: per-token recurrence), and its section
-"生产环境不支持" item 3 (chain verify).  This module only compiles that file with gcc and
+"生产环境不支持" item 3 (chain verify and the commit of the accepted draft state).  This module only compiles that file with gcc and
 marshals numpy float64 arrays into it.
 """
 from __future__ import annotations
@@ -57,6 +57,11 @@ def _bind(lib):
     lib.la_oracle_verify_chain.restype = ci
     lib.la_oracle_verify_tree.argtypes = [dp, dp, dp, dp, dp, ip, ip, dp, dp, ci, ci, ci, ci]
     lib.la_oracle_verify_tree.restype = ci
+    lib.la_oracle_extend_tracked.argtypes = [dp, dp, dp, dp, dp, ip, ip, up, ip, ip, dp, ci, ci,
+                                             ci, ci]
+    lib.la_oracle_extend_tracked.restype = ci
+    lib.la_oracle_commit_accepted.argtypes = [dp, ip, dp, ip, ci, ci, ci, ci]
+    lib.la_oracle_commit_accepted.restype = ci
     return lib
 
 
@@ -121,6 +126,38 @@ def extend(q, k, v, slopes_, pool, state_idx, cu_seqlens, prefix_mask, H: int, D
     return out, pool_c
 
 
+def extend_tracked(q, k, v, slopes_, pool, state_idx, cu_seqlens, prefix_mask, track_lens,
+                   track_idx, H: int, D: int, nthreads: int | None = None, lib=None):
+    """Packed varlen extend with state tracking: as extend(), and for every request b with
+    track_lens[b] >= 0 the state after its first track_lens[b] tokens is also written to slot
+    track_idx[b].  Returns (out, pool_after); raises ValueError on a track length outside
+    [-1, length] or a track slot that is the request's own slot."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T = q.shape[0]
+    assert q.shape == (T, H * D) and k.shape == q.shape and v.shape == q.shape
+    s = _f64(slopes_)
+    pool_c = _f64(pool).copy()
+    idx = _i32(state_idx)
+    cu = _i32(cu_seqlens)
+    pm = np.ascontiguousarray(np.asarray(prefix_mask, dtype=np.uint8))
+    tl = _i32(track_lens)
+    ti = _i32(track_idx)
+    B = idx.shape[0]
+    assert cu.shape == (B + 1,) and pm.shape == (B,) and tl.shape == (B,) and ti.shape == (B,)
+    assert all(0 <= int(ti[b]) < pool_c.shape[0] for b in range(B) if tl[b] >= 0)
+    out = np.zeros((T, H * D), dtype=np.float64)
+    rc = (lib or _load()).la_oracle_extend_tracked(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+        _ptr(s, ctypes.c_double), _ptr(pool_c, ctypes.c_double), _ptr(idx, ctypes.c_int32),
+        _ptr(cu, ctypes.c_int32), _ptr(pm, ctypes.c_uint8), _ptr(tl, ctypes.c_int32),
+        _ptr(ti, ctypes.c_int32), _ptr(out, ctypes.c_double), B, H, D,
+        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("track_lens must lie in [-1, request length] and track slots must not "
+                         "be the request's own slot")
+    return out, pool_c
+
+
 def decode(q, k, v, slopes_, pool, state_idx, H: int, D: int, nthreads: int | None = None,
            lib=None):
     """One decode token per request.  q, k, v: [B, H*D].  Returns (out [B, H*D], pool_after)."""
@@ -180,3 +217,22 @@ def verify_tree(q, k, v, slopes_, pool, state_idx, parents, N: int, H: int, D: i
     if rc != 0:
         raise ValueError("parents must satisfy -1 <= parents[b, t] < t")
     return out, inter
+
+
+def commit_accepted(inter, accept_idx, pool, state_idx, lib=None) -> np.ndarray:
+    """Accepted-state commit: returns a copy of ``pool`` in which slot state_idx[b] holds
+    inter[b, accept_idx[b]] for every b with accept_idx[b] >= 0.  inter: [B, N, H, D, D];
+    pool: [num_slots, H, D, D].  Raises ValueError if an index is outside [-1, N-1]."""
+    inter_c = _f64(inter)
+    acc = _i32(accept_idx)
+    idx = _i32(state_idx)
+    pool_c = _f64(pool).copy()
+    B, N, H, D = inter_c.shape[0], inter_c.shape[1], inter_c.shape[2], inter_c.shape[3]
+    assert acc.shape == (B,) and idx.shape == (B,) and pool_c.shape[1:] == (H, D, D)
+    assert B == 0 or (idx.min() >= 0 and idx.max() < pool_c.shape[0])
+    rc = (lib or _load()).la_oracle_commit_accepted(
+        _ptr(inter_c, ctypes.c_double), _ptr(acc, ctypes.c_int32), _ptr(pool_c, ctypes.c_double),
+        _ptr(idx, ctypes.c_int32), B, N, H, D)
+    if rc != 0:
+        raise ValueError("accept_idx must satisfy -1 <= accept_idx[b] < N")
+    return pool_c

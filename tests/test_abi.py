@@ -84,6 +84,12 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 0, 0, 1, 128, 0, n, 0, n) == 0
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 0, 1, 128, n) == 0
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 0, 1, 1, 128, n) == 0
+    # accepted-state commit: same rules
+    assert lib.la_commit_accepted(n, n, n, 1, n, 1, 1, 1, 64, n) == 2
+    assert lib.la_commit_accepted(n, n, n, 1, n, 1, 0, 1, 128, n) == 1
+    assert lib.la_commit_accepted(n, n, n, 0, n, 1, 1, 1, 128, n) == 1
+    assert lib.la_commit_accepted(n, n, n, 1, n, 1, 1, 1, 128, n) == 1
+    assert lib.la_commit_accepted(n, n, n, 1, n, 0, 1, 1, 128, n) == 0
 
 
 def test_status_strings(lib):
