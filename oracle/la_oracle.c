@@ -15,7 +15,11 @@
  *       start from a state injected into the state pool; the slope rule
  *       slopes * (1 - layer_id/(L-1) + 1e-5), and slopes * (1 + 1e-5) when L = 1.
  *   [LA-page §生产环境不支持 item 3]  chain (topk = 1) target verify: every draft token continues
- *       from the previous position's state.
+ *       from the previous position's state; once the target model has accepted some draft
+ *       tokens, the state after the last accepted one becomes the request's state.
+ *   [LA-page §额外覆盖]  "extra coverage: state tracking": during a prefill, the state at the
+ *       track_len-th token is also copied into a separate track slot, while the request's own
+ *       slot still receives the final state and every other slot is left alone.
  *   [LA-page §Next Work, item 2]  tree verify: each draft token forks from the state saved for
  *       its parent, not from the previous position of the chain.
  *
@@ -28,6 +32,10 @@
  *   - decay is applied before the outer product is added, so the current token has weight 1;
  *   - a request whose prefix flag is 0 starts from the zero state and never reads its slot;
  *   - the final state is written back for every request, including zero-length ones;
+ *   - state tracking: "the state at the track_len-th token" is the state after the first
+ *     track_len tokens of this call (track_len counts the call's new tokens, 0 meaning the
+ *     initial state); -1 means no snapshot; the track slot is a slot of the same pool and must
+ *     not be the request's own slot;
  *   - chain verify leaves the pool untouched and records the state after each draft token;
  *   - tree verify: parent[t] in [-1, t-1], -1 meaning the request's pool state; the state after
  *     token t is the recurrence applied to token t from the state after its parent.
@@ -94,6 +102,8 @@ typedef struct {
     const uint8_t *prefix_mask;   /* [B]   (extend) */
     double *out;                  /* [T][H*D] */
     double *inter;                /* [B][N][H][D][D] (verify) */
+    const int32_t *track_lens;    /* [B] or NULL (extend with state tracking) */
+    const int32_t *track_idx;     /* [B] or NULL */
     int B, H, D, N;
     int nthreads;
     int tid;
@@ -113,8 +123,18 @@ static void run_pair(const job_t *a, int b, int h)
             memset(S, 0, sizeof(double) * dd);
         const int t0 = a->cu_seqlens[b], n = a->cu_seqlens[b + 1] - t0;
         const size_t off = (size_t)t0 * row + (size_t)h * D;
-        recur(S, D, a->slopes[h], n, a->q + off, a->k + off, a->v + off, row, a->out + off,
+        /* [LA-page §额外覆盖] state tracking: once the first track_len tokens are processed,
+         * the state of that moment is copied into the track slot; the run then goes on. */
+        const int tl = a->track_lens ? a->track_lens[b] : -1;
+        const int n1 = tl >= 0 ? tl : n;
+        recur(S, D, a->slopes[h], n1, a->q + off, a->k + off, a->v + off, row, a->out + off,
               NULL, 0);
+        if (tl >= 0) {
+            memcpy(a->pool + ((size_t)a->track_idx[b] * H + h) * dd, S, sizeof(double) * dd);
+            const size_t off2 = off + (size_t)n1 * row;
+            recur(S, D, a->slopes[h], n - n1, a->q + off2, a->k + off2, a->v + off2, row,
+                  a->out + off2, NULL, 0);
+        }
         memcpy(slot, S, sizeof(double) * dd); /* final state written back at the end */
     } else if (a->op == OP_DECODE) {
         memcpy(S, slot, sizeof(double) * dd);
@@ -187,6 +207,31 @@ int la_oracle_extend(const double *q, const double *k, const double *v, const do
     return run(&a);
 }
 
+/* Extend with state tracking: as la_oracle_extend, and for every request b with
+ * track_lens[b] >= 0 the state after its first track_lens[b] tokens (its initial state when 0,
+ * its final state when track_lens[b] is its length) is also written to pool slot track_idx[b].
+ * track_lens[b] == -1: no snapshot.  Returns -1 (and computes nothing) if some track_lens[b] is
+ * outside [-1, length of b] or a snapshot would go to the request's own slot. */
+int la_oracle_extend_tracked(const double *q, const double *k, const double *v,
+                             const double *slopes, double *pool, const int32_t *state_idx,
+                             const int32_t *cu_seqlens, const uint8_t *prefix_mask,
+                             const int32_t *track_lens, const int32_t *track_idx, double *out,
+                             int B, int H, int D, int nthreads)
+{
+    for (int b = 0; b < B; b++) {
+        const int tl = track_lens[b], n = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (tl < -1 || tl > n || (tl >= 0 && track_idx[b] == state_idx[b]))
+            return -1;
+    }
+    job_t a = {0};
+    a.op = OP_EXTEND;
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool;
+    a.state_idx = state_idx; a.cu_seqlens = cu_seqlens; a.prefix_mask = prefix_mask;
+    a.track_lens = track_lens; a.track_idx = track_idx;
+    a.out = out; a.B = B; a.H = H; a.D = D; a.N = 0; a.nthreads = nthreads;
+    return run(&a);
+}
+
 /* One-token decode: q, k, v, out are [B][H*D]; every request starts from its pool slot and the
  * slot is updated in place. */
 int la_oracle_decode(const double *q, const double *k, const double *v, const double *slopes,
@@ -251,4 +296,25 @@ int la_oracle_verify_chain(const double *q, const double *k, const double *v,
     a.state_idx = state_idx; a.inter = inter; a.out = out;
     a.B = B; a.H = H; a.D = D; a.N = N; a.nthreads = nthreads;
     return run(&a);
+}
+
+/* Accepted-state commit after a verify: for each request b with accept[b] >= 0, the pool slot
+ * state_idx[b] takes the state after draft token accept[b] (inter[b][accept[b]], all heads);
+ * accept[b] == -1 leaves the slot alone.  Returns -1 (and changes nothing) if some accept[b] is
+ * outside [-1, N-1]. */
+int la_oracle_commit_accepted(const double *inter, const int32_t *accept, double *pool,
+                              const int32_t *state_idx, int B, int N, int H, int D)
+{
+    for (int b = 0; b < B; b++)
+        if (accept[b] < -1 || accept[b] >= N)
+            return -1;
+    const size_t hdd = (size_t)H * D * D;
+    for (int b = 0; b < B; b++) {
+        int a = accept[b];
+        if (a < 0)
+            continue;
+        memcpy(pool + (size_t)state_idx[b] * hdd, inter + ((size_t)b * N + a) * hdd,
+               sizeof(double) * hdd);
+    }
+    return 0;
 }

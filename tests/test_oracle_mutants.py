@@ -48,11 +48,23 @@ MUTANTS = {
                           "        memset(S, 0, sizeof(double) * dd);\n"
                           "        const size_t off = (size_t)b * row + (size_t)h * D;"),
     "request_length_short": ("n = a->cu_seqlens[b + 1] - t0;", "n = a->cu_seqlens[b + 1] - t0 - 1;"),
-    "wrong_head_slope": ("recur(S, D, a->slopes[h], n,", "recur(S, D, a->slopes[0], n,"),
+    "wrong_head_slope": ("recur(S, D, a->slopes[h], n1,", "recur(S, D, a->slopes[0], n1,"),
     "tree_forks_from_previous": ("par < 0 ? root : inter + (((size_t)b * N + par) * H + h) * dd;",
                                  "(t == 0) ? root : inter + (((size_t)b * N + t - 1) * H + h) * dd;"),
     "tree_forks_from_root": ("par < 0 ? root : inter + (((size_t)b * N + par) * H + h) * dd;",
                              "root;"),
+    "commit_reads_first_token": ("pool + (size_t)state_idx[b] * hdd, inter + ((size_t)b * N + a) * hdd,",
+                                 "pool + (size_t)state_idx[b] * hdd, inter + ((size_t)b * N) * hdd,"),
+    "commit_skip_taken_as_zero": ("        if (a < 0)\n            continue;",
+                                  "        if (a < 0)\n            a = 0;"),
+    "commit_other_request": ("pool + (size_t)state_idx[b] * hdd, inter + ((size_t)b * N + a) * hdd,",
+                             "pool + (size_t)state_idx[b] * hdd, inter + ((size_t)(B - 1 - b) * N + a) * hdd,"),
+    "track_snapshot_one_late": ("const int n1 = tl >= 0 ? tl : n;",
+                                "const int n1 = tl >= 0 ? (tl < n ? tl + 1 : tl) : n;"),
+    "track_snapshot_to_own_slot": ("memcpy(a->pool + ((size_t)a->track_idx[b] * H + h) * dd, S,",
+                                   "memcpy(a->pool + ((size_t)a->state_idx[b] * H + h) * dd, S,"),
+    "track_rest_not_processed": ("recur(S, D, a->slopes[h], n - n1, a->q + off2,",
+                                 "recur(S, D, a->slopes[h], 0, a->q + off2,"),
 }
 
 

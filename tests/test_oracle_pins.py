@@ -303,3 +303,141 @@ def test_tree_verify_rejects_forward_parents():
     with pytest.raises(ValueError):
         oracle.verify_tree(q, q, q, [0.1], np.zeros((1, H, D, D)), [0],
                            np.array([[-2, 0, 1]], dtype=np.int32), 3, H, D)
+
+
+def test_commit_after_chain_verify_is_the_accepted_prefix_state():
+    """Committing draft token a of a chain verify leaves in the slot the closed-form state after
+    tokens 0..a; -1 leaves the slot as it was; slots no request names are untouched; and a decode
+    from the committed slot continues the sequence."""
+    H, D, B, N = 2, 6, 4, 4
+    q, k, v = rng_inputs(31, B * N, H, D)
+    slopes = np.array([0.4, 0.03])
+    pool = np.random.default_rng(32).standard_normal((7, H, D, D)) * 0.05
+    idx = np.array([5, 0, 3, 6], dtype=np.int32)
+    accept = np.array([2, -1, 0, 3], dtype=np.int32)
+    _, inter = oracle.verify_chain(q, k, v, slopes, pool, idx, N, H, D)
+    new_pool = oracle.commit_accepted(inter, accept, pool, idx)
+    for s in range(7):
+        if s not in idx:
+            np.testing.assert_array_equal(new_pool[s], pool[s])
+    for b in range(B):
+        a = int(accept[b])
+        if a < 0:
+            np.testing.assert_array_equal(new_pool[idx[b]], pool[idx[b]])
+            continue
+        rows = slice(b * N, b * N + a + 1)
+        for h in range(H):
+            sl = slice(h * D, (h + 1) * D)
+            _, S = closed_form(q[rows, sl], k[rows, sl], v[rows, sl], slopes[h], pool[idx[b], h], D)
+            np.testing.assert_allclose(new_pool[idx[b], h], S, rtol=1e-13, atol=1e-15)
+    # one more token from the committed state equals the recurrence over a + 2 tokens
+    qn, kn, vn = rng_inputs(33, B, H, D)
+    d_out, d_pool = oracle.decode(qn, kn, vn, slopes, new_pool, idx, H, D)
+    for b in (0, 2, 3):
+        a = int(accept[b])
+        rows = list(range(b * N, b * N + a + 1))
+        for h in range(H):
+            sl = slice(h * D, (h + 1) * D)
+            qq = np.vstack([q[rows, sl], qn[b, sl]])
+            kk = np.vstack([k[rows, sl], kn[b, sl]])
+            vv = np.vstack([v[rows, sl], vn[b, sl]])
+            o, S = closed_form(qq, kk, vv, slopes[h], pool[idx[b], h], D)
+            np.testing.assert_allclose(d_out[b, sl], o[-1], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(d_pool[idx[b], h], S, rtol=1e-13, atol=1e-15)
+
+
+def test_commit_after_tree_verify_is_the_root_path_state():
+    H, D, B, N = 1, 5, 3, 6
+    q, k, v = rng_inputs(34, B * N, H, D)
+    slopes = np.array([0.2])
+    pool = np.random.default_rng(35).standard_normal((4, H, D, D)) * 0.05
+    idx = np.array([1, 3, 0], dtype=np.int32)
+    parents = np.array([[-1, 0, 0, 1, 2, 2]] * B, dtype=np.int32)
+    accept = np.array([4, 3, 5], dtype=np.int32)
+    _, inter = oracle.verify_tree(q, k, v, slopes, pool, idx, parents, N, H, D)
+    new_pool = oracle.commit_accepted(inter, accept, pool, idx)
+    np.testing.assert_array_equal(new_pool[2], pool[2])
+    for b in range(B):
+        path, x = [], int(accept[b])
+        while x >= 0:
+            path.append(b * N + x)
+            x = parents[b, x]
+        path = path[::-1]
+        _, S = closed_form(q[path], k[path], v[path], slopes[0], pool[idx[b], 0], D)
+        np.testing.assert_allclose(new_pool[idx[b], 0], S, rtol=1e-13, atol=1e-15)
+
+
+def test_commit_rejects_out_of_range_index():
+    inter = np.zeros((1, 3, 1, 4, 4))
+    pool = np.ones((2, 1, 4, 4))
+    for bad in (3, -2):
+        with pytest.raises(ValueError):
+            oracle.commit_accepted(inter, [bad], pool, [1])
+
+
+def _tracked_case(seed=41):
+    H, D = 2, 6
+    lens = [9, 5, 0, 12, 7, 4]
+    tls = [4, 0, 0, 12, -1, 0]
+    pm = [1, 0, 0, 1, 1, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v = rng_inputs(seed, int(cu[-1]), H, D)
+    slopes = np.array([0.3, 0.05])
+    S = 16
+    pool = np.full((S, H, D, D), 54321.0)
+    r = np.random.default_rng(seed + 1)
+    idx = np.array([3, 7, 1, 12, 0, 9], dtype=np.int32)
+    tidx = np.array([5, 2, 15, 8, 6, 11], dtype=np.int32)
+    for b in range(len(lens)):
+        pool[idx[b]] = r.standard_normal((H, D, D)) * 0.05 if pm[b] else np.nan
+    return H, D, lens, tls, pm, cu, q, k, v, slopes, pool, idx, tidx
+
+
+def test_tracking_snapshot_is_the_state_after_track_len_tokens():
+    """The track slot holds the closed-form state after the first track_len tokens (the initial
+    state for 0, the final state for the full length); outputs and final states are those of a
+    plain extend; slots that nothing names keep their bytes; -1 writes no snapshot."""
+    H, D, lens, tls, pm, cu, q, k, v, slopes, pool, idx, tidx = _tracked_case()
+    out, got = oracle.extend_tracked(q, k, v, slopes, pool, idx, cu, pm, tls, tidx, H, D)
+    out_p, got_p = oracle.extend(q, k, v, slopes, pool, idx, cu, pm, H, D)
+    np.testing.assert_array_equal(out, out_p)
+    np.testing.assert_array_equal(got[idx], got_p[idx])
+    snap = {int(tidx[b]) for b in range(len(lens)) if tls[b] >= 0}
+    for s in range(pool.shape[0]):
+        if s not in snap and s not in idx:
+            np.testing.assert_array_equal(got[s], pool[s])
+    np.testing.assert_array_equal(got[tidx[4]], pool[tidx[4]])  # track_len -1: untouched
+    for b in range(len(lens)):
+        if tls[b] < 0:
+            continue
+        rows = slice(int(cu[b]), int(cu[b]) + tls[b])
+        for h in range(H):
+            sl = slice(h * D, (h + 1) * D)
+            S0 = pool[idx[b], h] if pm[b] else np.zeros((D, D))
+            _, S = closed_form(q[rows, sl], k[rows, sl], v[rows, sl], slopes[h], S0, D)
+            np.testing.assert_allclose(got[tidx[b], h], S, rtol=1e-13, atol=1e-15)
+
+
+def test_tracking_snapshot_equals_verify_intermediate_state():
+    """The check the page describes: the snapshot at track_len equals the per-token recurrence's
+    state at that moment, here chain verify's state after draft token track_len - 1."""
+    H, D, lens, tls, pm, cu, q, k, v, slopes, pool, idx, tidx = _tracked_case(43)
+    _, got = oracle.extend_tracked(q, k, v, slopes, pool, idx, cu, pm, tls, tidx, H, D)
+    for b in (0, 3):
+        n = lens[b]
+        rows = slice(int(cu[b]), int(cu[b]) + n)
+        _, inter = oracle.verify_chain(q[rows], k[rows], v[rows], slopes, pool, [idx[b]], n, H, D)
+        np.testing.assert_allclose(got[tidx[b]], inter[0, tls[b] - 1], rtol=1e-13, atol=1e-15)
+
+
+def test_tracking_rejects_bad_track_lengths_and_own_slot():
+    H, D, lens, tls, pm, cu, q, k, v, slopes, pool, idx, tidx = _tracked_case()
+    for b, bad_tl in ((0, 10), (1, -2), (2, 1)):
+        t = list(tls)
+        t[b] = bad_tl
+        with pytest.raises(ValueError):
+            oracle.extend_tracked(q, k, v, slopes, pool, idx, cu, pm, t, tidx, H, D)
+    ti = tidx.copy()
+    ti[3] = idx[3]
+    with pytest.raises(ValueError):
+        oracle.extend_tracked(q, k, v, slopes, pool, idx, cu, pm, tls, ti, H, D)
