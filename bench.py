@@ -2,13 +2,17 @@
 """Benchmark of the seg_la hot path on GB300: tokens/s and the fraction of the HBM/tensor roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload decode|varlen_extend|long_prefill|verify] [--headline-only]
+                    [--workload NAME] [--headline-only]
+    python bench.py --profile-calls C [--workload NAME | --profile-case CASE]   (untimed)
 
 A step is one call of the path over one batch of the chosen workload (inputs resident in HBM):
   decode         256 requests x 1 token, H=16, layer 3 of L=8, 1024-slot pool   (default)
   varlen_extend  8 requests, lengths uniform in [512, 4096], H=16, layer 0 of L=4
   long_prefill   1 request of 32768 tokens, H=32, layer 5 of L=12
   verify         128 requests x 5 draft tokens, H=64, layer 10 of L=20, 512-slot pool
+  verify_tree    the same requests with an 8-token binary draft tree each
+  varlen_extend_tracked  varlen_extend plus a state-tracking snapshot per request
+  verify_commit  verify followed by the accepted-state commit (two library calls)
 Every workload's inputs exceed the 129 MB L2, so no flush is needed between steps.  With N > 1
 (torchrun), every rank runs its own replica of the workload (weak scaling, no collective on the
 data path); timing is bracketed by a barrier and the slowest rank's time is reported.
@@ -49,6 +53,8 @@ KERNEL_SOURCE = {
     "varlen_extend": "la_extend_tc.cu",
     "long_prefill": "la_extend_tc.cu",
     "verify_tree": "la_recurrent.cu",
+    "varlen_extend_tracked": "la_extend_tc.cu",
+    "verify_commit": "la_recurrent.cu",
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
@@ -56,6 +62,13 @@ KERNEL_NAME = {
     "varlen_extend": "extend_chunked_kernel",
     "long_prefill": "extend_chunked_kernel",
     "verify_tree": "recurrent_kernel<3>",
+    "varlen_extend_tracked": "extend_chunked_kernel",
+    "verify_commit": "recurrent_kernel<1>",
+}
+# Small cases of the same kernels for multi-pass ncu captures (--profile-calls); a few GB at most.
+PROFILE_CASES = {
+    "verify_b32": lambda: workloads.verify_chain(0, B=32, num_slots=64),
+    "verify_tree_b32": lambda: workloads.verify_tree(0, B=32, num_slots=64),
 }
 
 
@@ -118,12 +131,17 @@ def algorithmic(w) -> dict:
         # fork re-reads from the intermediate buffer are not counted
         tokens = w.B * w.N
         byts = w.B * H * D * D * 4 * (1 + w.N) + 4 * w.B * w.N * H * D * 2
+        if w.accept_idx is not None:
+            # the commit: each accepted state read from the intermediate buffer, written to its slot
+            byts += 2 * int((w.accept_idx >= 0).sum()) * H * D * D * 4
         flops = tokens * H * 4 * D * D
         issued = flops
     else:
         tokens = w.T
         n_prefix = int(w.prefix_mask.sum())
         byts = 4 * w.T * H * D * 2 + (n_prefix + w.B) * H * D * D * 4
+        if w.track_lens is not None:
+            byts += int((w.track_lens >= 0).sum()) * H * D * D * 4   # the snapshots
         flops = w.T * H * 4 * D * D           # the recurrence's own 4 d^2 per token-head
         issued = None                         # filled from the kernel's chunk geometry
     return {"tokens": tokens, "bytes": byts, "flops": flops, "issued_flops": issued}
@@ -237,7 +255,7 @@ class ClockSampler:
 class GpuCase:
     """Device-resident inputs and a step() that makes exactly one library call."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, name):
         import lightning_attention_gb300 as la
         self.la = la
         self.w = w
@@ -248,8 +266,7 @@ class GpuCase:
         self.idx = w.state_idx.to(dev)
         self.out = torch.empty_like(self.q)
         self.launches_per_step = 1
-        self.kernel = KERNEL_NAME[{"decode": "decode", "verify": "verify",
-                                   "tree": "verify_tree"}.get(w.kind, "varlen_extend")]
+        self.kernel = KERNEL_NAME[name]
         if w.kind == "extend":
             self.cu = w.cu_seqlens.to(dev)
             self.pm = w.prefix_mask.to(dev)
@@ -259,10 +276,21 @@ class GpuCase:
                 # long requests split into segments: block-state kernel, then the extend kernel
                 self.launches_per_step = 2
                 self.kernel = "block_state_kernel + extend_chunked_kernel (one la_extend call)"
+            self.track = None
+            if w.track_lens is not None:
+                # one more launch: the within-chunk rest of each snapshot
+                self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
+                self.launches_per_step += 1
+                self.kernel += " + recurrent_kernel<4> (state tracking)"
         if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
         if w.kind == "tree":
             self.parents = w.parents.to(dev)
+        self.accept = None
+        if w.accept_idx is not None:
+            self.accept = w.accept_idx.to(dev)
+            self.launches_per_step += 1
+            self.kernel += " + commit_kernel"
 
     def step(self, q=None, k=None, v=None, idx=None):
         la, w = self.la, self.w
@@ -275,9 +303,15 @@ class GpuCase:
         elif w.kind == "verify":
             la.verify_chain(q, k, v, self.slopes, self.pool, idx, w.N,
                             inter_states=self.inter, out=self.out)
+            if self.accept is not None:
+                la.commit_accepted(self.inter, self.accept, self.pool, idx)
         elif w.kind == "tree":
             la.verify_tree(q, k, v, self.slopes, self.pool, idx, self.parents, w.N,
                            inter_states=self.inter, out=self.out)
+        elif self.track is not None:
+            la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=self.out,
+                      max_seqlen=self.max_seqlen, track_lens=self.track[0],
+                      track_state_idx=self.track[1])
         else:
             la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=self.out,
                       max_seqlen=self.max_seqlen)
@@ -288,7 +322,7 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
     import lightning_attention_gb300 as la
     w = make_workload(name, rank_seed(0, rank))
     geo = algorithmic(w)
-    case = GpuCase(w, dev)
+    case = GpuCase(w, dev, name)
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
         case.step()
@@ -428,8 +462,11 @@ def run_oracle_sample(w, sample, threads):
         q, k, v = (t[:rows].float().numpy().astype(np.float64) for t in (w.q, w.k, w.v))
         pool = w.prefix_states[:B].double().numpy()
         t0 = time.perf_counter()
-        oracle.verify_chain(q, k, v, s, pool, np.arange(B, dtype=np.int32), w.N, w.H, D,
-                            nthreads=threads)
+        _, inter = oracle.verify_chain(q, k, v, s, pool, np.arange(B, dtype=np.int32), w.N, w.H,
+                                       D, nthreads=threads)
+        if w.accept_idx is not None:
+            oracle.commit_accepted(inter, w.accept_idx[:B].numpy(), pool,
+                                   np.arange(B, dtype=np.int32))
         return time.perf_counter() - t0
     if sample["kind"] == "tree":
         B = sample["B"]
@@ -455,15 +492,24 @@ def run_oracle_sample(w, sample, threads):
     sub_cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     pool = w.prefix_states[reqs].double().numpy()
     pm = w.prefix_mask.numpy()[reqs]
+    nr = len(reqs)
+    if w.track_lens is not None:
+        # snapshots go to slots nr .. 2 nr - 1 of the sample's pool
+        pool = np.concatenate([pool, np.zeros_like(pool)])
+        t0 = time.perf_counter()
+        oracle.extend_tracked(q, k, v, s, pool, np.arange(nr, dtype=np.int32), sub_cu, pm,
+                              w.track_lens.numpy()[reqs], np.arange(nr, 2 * nr, dtype=np.int32),
+                              w.H, D, nthreads=threads)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle.extend(q, k, v, s, pool, np.arange(len(reqs), dtype=np.int32), sub_cu, pm, w.H, D,
+    oracle.extend(q, k, v, s, pool, np.arange(nr, dtype=np.int32), sub_cu, pm, w.H, D,
                   nthreads=threads)
     return time.perf_counter() - t0
 
 
 ORACLE_BUDGET = {  # (request, head) pairs or token-heads per sample: ~1-10 s of fp64 CPU work
     "decode": 4096, "verify": 64 * 5 * 16, "varlen_extend": 16 * 2400, "long_prefill": 32 * 1200,
-    "verify_tree": 64 * 8 * 8}
+    "verify_tree": 64 * 8 * 8, "varlen_extend_tracked": 16 * 2400, "verify_commit": 64 * 5 * 16}
 
 
 def cpu_baseline(name, w, threads):
@@ -508,10 +554,16 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=list(KERNEL_SOURCE), default=HEADLINE)
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="untimed: make this many library calls on --workload (or "
+                         "--profile-case) on cuda:0 and exit; the command an ncu capture runs")
+    ap.add_argument("--profile-case", choices=list(PROFILE_CASES), default=None)
     args = ap.parse_args()
 
     if args.impl == "reference":
         return main_reference(args)
+    if args.profile_calls > 0:
+        return main_profile(args)
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -565,6 +617,26 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def main_profile(args):
+    """The workload's step, args.profile_calls times, with nothing timed or printed but a final
+    status line: what an ncu capture of one kernel runs (-k / -s / -c select the launch)."""
+    import lightning_attention_gb300 as la
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.profile_case:
+        w, name = PROFILE_CASES[args.profile_case](), args.profile_case
+        kname = {"verify_b32": "verify", "verify_tree_b32": "verify_tree"}[name]
+    else:
+        w, name = make_workload(args.workload, 0), args.workload
+        kname = name
+    case = GpuCase(w, dev, kname)
+    for _ in range(args.profile_calls):
+        case.step()
+    la.poll_error()
+    torch.cuda.synchronize(dev)
+    print(f"profile run ok: {w.name}, {args.profile_calls} calls", flush=True)
 
 
 def calibrated_sample(name, w, threads, seconds_per_step):

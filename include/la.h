@@ -116,6 +116,32 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
                     la_stream stream);
 
 /*
+ * la_extend_tracked -- la_extend plus a state-tracking snapshot per request ([LA-page §额外覆盖],
+ * the extra-buffer state tracking of a prefill: at the track_len-th token the running state is
+ * copied into a track slot, while the request's own slot still receives the final state and no
+ * other slot is written).
+ *   track_lens       device, int32 [B]: the snapshot is the state after the first track_lens[b]
+ *                    tokens of request b in this call (0: its initial state -- the prefix state
+ *                    or zero; its length: its final state); -1: no snapshot for b
+ *   track_state_idx  device, int32 [B]: the pool slot that receives b's snapshot (ignored when
+ *                    track_lens[b] == -1)
+ * Both NULL: exactly la_extend.  One NULL: LA_ERR_INVALID.  Other arguments, outputs, the final
+ * states and the errors are those of la_extend.  A track length outside [-1, length] or a track
+ * slot that is out of range or equal to the request's own slot skips that snapshot and is
+ * reported by la_poll_error as LA_ERR_DEVICE_INPUT.  Track slots must differ from every slot the
+ * call reads or writes otherwise and from one another (not checked: overlapping slots race).
+ * Launches: la_extend's kernels, then one token-serial pass that advances each snapshot from the
+ * chunk boundary before it (chunks are 128 tokens) to its token.
+ */
+la_status la_extend_tracked(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                            const float *slopes, float *state_pool, int num_slots,
+                            const int32_t *state_idx, const int32_t *cu_seqlens,
+                            const uint8_t *prefix_mask, const int32_t *track_lens,
+                            const int32_t *track_state_idx, la_bf16 *out, int B, int T, int H,
+                            int D, int max_seqlen, void *workspace, size_t workspace_bytes,
+                            la_stream stream);
+
+/*
  * la_extend_workspace_size -- bytes of device scratch la_extend would use for a batch of this
  * shape on the current device (0 when it would not split any request).  Host only, no device work
  * beyond one cached attribute query.  Arguments as for la_extend; *bytes is written on success.
@@ -224,8 +250,9 @@ la_status la_commit_accepted(const float *inter_states, const int32_t *accept_id
 /*
  * la_poll_error -- synchronise `stream`, then read and clear the current device's error word.
  * Returns LA_ERR_TIMEOUT if a bounded device wait ran out, LA_ERR_DEVICE_INPUT if a kernel found
- * a slot index out of range, inconsistent cu_seqlens, a tree parent or commit index out of range,
- * LA_ERR_CUDA if the stream reports a CUDA error, else LA_OK.  This is the one call that blocks the host.
+ * a slot index out of range, inconsistent cu_seqlens, a tree parent, commit index or track entry
+ * out of range, LA_ERR_CUDA if the stream reports a CUDA error, else LA_OK.  This is the one call
+ * that blocks the host.
  */
 la_status la_poll_error(la_stream stream);
 

@@ -23,7 +23,7 @@ _lib = None
 STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
           4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
 
-EXPORTS = ("la_slopes", "la_extend", "la_extend_workspace_size", "la_decode", "la_verify_chain",
+EXPORTS = ("la_slopes", "la_extend", "la_extend_tracked", "la_extend_workspace_size", "la_decode", "la_verify_chain",
            "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
            "la_set_wait_limit")
 
@@ -66,6 +66,9 @@ def load():
         lib.la_verify_chain.restype = ip
         lib.la_verify_tree.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, vp]
         lib.la_verify_tree.restype = ip
+        lib.la_extend_tracked.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, vp, vp, ip, ip,
+                                          ip, ip, ip, vp, sz, vp]
+        lib.la_extend_tracked.restype = ip
         lib.la_commit_accepted.argtypes = [vp, vp, vp, ip, vp, ip, ip, ip, ip, vp]
         lib.la_commit_accepted.restype = ip
         lib.la_poll_error.argtypes = [vp]
@@ -144,13 +147,18 @@ def _cached_workspace(dev: torch.device, nbytes: int) -> torch.Tensor:
 
 
 def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
-           max_seqlen: int | None = None, workspace=None):
+           max_seqlen: int | None = None, workspace=None, track_lens=None, track_state_idx=None):
     """Packed varlen extend (la_extend).  q, k, v: bf16 [T, H*D]; state_pool fp32
     [S, H, D, D] updated in place; returns out bf16 [T, H*D].
 
     workspace: None lets the binding supply the scratch la_extend_workspace_size asks for (a
     cached per-device buffer); False runs without scratch (no sequence split); a uint8 CUDA
-    tensor is used as given."""
+    tensor is used as given.  Under CUDA-graph capture pass max_seqlen and a workspace tensor
+    (or make one eager call of the same shape first), so that nothing is allocated.
+
+    track_lens, track_state_idx: int32 [B] device tensors (both or neither) select
+    la_extend_tracked: the state after the first track_lens[b] tokens of request b is also
+    written to slot track_state_idx[b] (-1: no snapshot)."""
     dev = q.device
     T = q.shape[0]
     num_slots, H, D, D2 = state_pool.shape
@@ -167,6 +175,11 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     _need(out, "out", torch.bfloat16, dev, (T, H * D))
     if max_seqlen is None:
         max_seqlen = T
+    if (track_lens is None) != (track_state_idx is None):
+        raise ValueError("track_lens and track_state_idx go together")
+    if track_lens is not None:
+        _need(track_lens, "track_lens", torch.int32, dev, (B,))
+        _need(track_state_idx, "track_state_idx", torch.int32, dev, (B,))
     with torch.cuda.device(dev):
         if workspace is None:
             nbytes = extend_workspace_size(B, T, H, D, int(max_seqlen))
@@ -178,10 +191,18 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
             _need(ws, "workspace", torch.uint8, dev)
         ws_ptr = _ptr(ws)
         ws_bytes = ws.numel() if ws is not None else 0
-        st = load().la_extend(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool), num_slots,
-                              _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask), _ptr(out), B, T,
-                              H, D, int(max_seqlen), ws_ptr, ws_bytes, _stream_handle(dev))
-    _check("la_extend", st)
+        if track_lens is None:
+            st = load().la_extend(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                  num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),
+                                  _ptr(out), B, T, H, D, int(max_seqlen), ws_ptr, ws_bytes,
+                                  _stream_handle(dev))
+        else:
+            st = load().la_extend_tracked(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_),
+                                          _ptr(state_pool), num_slots, _ptr(state_idx),
+                                          _ptr(cu_seqlens), _ptr(prefix_mask), _ptr(track_lens),
+                                          _ptr(track_state_idx), _ptr(out), B, T, H, D,
+                                          int(max_seqlen), ws_ptr, ws_bytes, _stream_handle(dev))
+    _check("la_extend" if track_lens is None else "la_extend_tracked", st)
     return out
 
 
@@ -214,6 +235,11 @@ def extend_noalloc(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_m
     _need(out, "out", torch.bfloat16, dev, (T, H * D))
     if max_seqlen is None:
         max_seqlen = T
+    if (track_lens is None) != (track_state_idx is None):
+        raise ValueError("track_lens and track_state_idx go together")
+    if track_lens is not None:
+        _need(track_lens, "track_lens", torch.int32, dev, (B,))
+        _need(track_state_idx, "track_state_idx", torch.int32, dev, (B,))
     with torch.cuda.device(dev):
         st = lib.la_extend_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                    num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),

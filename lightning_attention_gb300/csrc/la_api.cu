@@ -109,7 +109,7 @@ la_status la_poll_error(la_stream stream) {
     }
     if (word & la::ERR_BIT_TIMEOUT) return LA_ERR_TIMEOUT;
     if (word & (la::ERR_BIT_SLOT_RANGE | la::ERR_BIT_SEQLENS | la::ERR_BIT_PARENTS |
-                la::ERR_BIT_ACCEPT))
+                la::ERR_BIT_ACCEPT | la::ERR_BIT_TRACK))
         return LA_ERR_DEVICE_INPUT;
     return LA_OK;
 }
@@ -220,11 +220,16 @@ la_status la_commit_accepted(const float *inter_states, const int32_t *accept_id
     return launch_status(la::launch_commit(p, static_cast<cudaStream_t>(stream)));
 }
 
-la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
-                    float *state_pool, int num_slots, const int32_t *state_idx,
-                    const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
-                    int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
-                    la_stream stream) {
+}  // extern "C"
+
+namespace {
+
+la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                      float *state_pool, int num_slots, const int32_t *state_idx,
+                      const int32_t *cu_seqlens, const uint8_t *prefix_mask,
+                      const int32_t *track_lens, const int32_t *track_state_idx, la_bf16 *out,
+                      int B, int T, int H, int D, int max_seqlen, void *workspace,
+                      size_t workspace_bytes, la_stream stream) {
     if (B < 0 || T < 0 || H < 1 || D < 1 || num_slots < 1 || max_seqlen < 0)
         return LA_ERR_INVALID;
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
@@ -260,6 +265,8 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     p.nblk = 0;
     p.ws = nullptr;
     p.lpt = (B > 1 && B <= 256) ? 1 : 0;
+    p.track_lens = track_lens;
+    p.track_idx = track_state_idx;
     if (workspace != nullptr && aligned16(workspace) && T > 0) {
         int sms = 0;
         if ((st = num_sms(&sms)) != LA_OK) return st;
@@ -277,7 +284,52 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
-    return launch_status(la::launch_extend_chunked(p, s));
+    if (track_lens == nullptr) return launch_status(la::launch_extend_chunked(p, s));
+    if (la::launch_extend_chunked(p, s) != cudaSuccess) return LA_ERR_CUDA;
+    // the within-chunk rest of each snapshot, after the extend on the same stream
+    la::RecurParams r{};
+    r.k = p.k;
+    r.v = p.v;
+    r.q = p.q;
+    r.slopes = slopes;
+    r.pool = state_pool;
+    r.state_idx = state_idx;
+    r.cu_seqlens = cu_seqlens;
+    r.track_lens = track_lens;
+    r.track_idx = track_state_idx;
+    r.err = p.err;
+    r.B = B;
+    r.H = H;
+    r.T = T;
+    r.num_slots = num_slots;
+    return launch_status(la::launch_recurrent(la::RECUR_TRACK, r, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                    float *state_pool, int num_slots, const int32_t *state_idx,
+                    const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out, int B,
+                    int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
+                    la_stream stream) {
+    return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
+                       nullptr, nullptr, out, B, T, H, D, max_seqlen, workspace, workspace_bytes,
+                       stream);
+}
+
+la_status la_extend_tracked(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
+                            const float *slopes, float *state_pool, int num_slots,
+                            const int32_t *state_idx, const int32_t *cu_seqlens,
+                            const uint8_t *prefix_mask, const int32_t *track_lens,
+                            const int32_t *track_state_idx, la_bf16 *out, int B, int T, int H,
+                            int D, int max_seqlen, void *workspace, size_t workspace_bytes,
+                            la_stream stream) {
+    if ((track_lens == nullptr) != (track_state_idx == nullptr)) return LA_ERR_INVALID;
+    return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
+                       track_lens, track_state_idx, out, B, T, H, D, max_seqlen, workspace,
+                       workspace_bytes, stream);
 }
 
 la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, size_t *bytes) {

@@ -62,7 +62,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int C = 128;              // chunk length in tokens
+constexpr int C = kChunk;           // chunk length in tokens
 constexpr int DV = 64;              // v columns per CTA
 constexpr int NV = kHeadDim / DV;   // v blocks per head
 constexpr int kEpiWarps = 8;
@@ -212,6 +212,16 @@ __device__ __forceinline__ void store_p_block(uint8_t *sP, int i, int cb, const 
         *reinterpret_cast<uint4 *>(prow + chunk * 16) =
             make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
     }
+}
+
+// This thread's share of a state (row i, columns col0 .. col0 + 31) into pool slot `slot`.
+__device__ __forceinline__ void store_state_row(float *pool, int slot, int H, int h, int i,
+                                                int col0, const float *S) {
+    float *dst = pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+        *reinterpret_cast<float4 *>(dst + 4 * x) =
+            make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -466,6 +476,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float *gstate =
             p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
+        // State tracking: the snapshot after the first tl tokens of the request starts as the
+        // state at request chunk boundary cb (tl rounded down to a chunk, or the request's end
+        // when tl is its length); the CTA whose segment holds that boundary stores it, as the
+        // state before its local chunk `snap`.  RECUR_TRACK adds the tokens between cb and tl.
+        int snap = -1, tslot = 0;
+        if (p.track_lens != nullptr) {
+            const int tl = p.track_lens[b];
+            tslot = p.track_idx[b];
+            if (tl >= 0) {
+                if (tl > n_req || tslot < 0 || tslot >= p.num_slots || tslot == slot) {
+                    if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_TRACK);
+                } else {
+                    const int cb = tl == n_req ? (n_req + C - 1) / C : tl / C;
+                    const int lc = cb - (t0 - t_req0) / C;
+                    if ((lc >= 0 && lc < nchunks) || (lc == nchunks && last_seg)) snap = lc;
+                }
+            }
+        }
         const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)wg * 32u;
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
@@ -516,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 32; ++x) S[x] = 0.f;
             }
+            if (snap == 0) store_state_row(p.pool, tslot, H, h, i, col0, S);
             uint32_t w[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[x]);
@@ -598,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st32(t_s, w);
                 store_state_split(s_hi, s_lo, i, wg, S);
+                if (c + 1 == snap) store_state_row(p.pool, tslot, H, h, i, col0, S);
                 tmem_st_wait();
             }
             fence_proxy_async_smem();

@@ -14,12 +14,21 @@ enum : unsigned int {
     ERR_BIT_SEQLENS = 4u,       // cu_seqlens decreasing or past T
     ERR_BIT_PARENTS = 8u,       // tree-verify parent index outside [-1, t-1]
     ERR_BIT_ACCEPT = 16u,       // commit index outside [-1, N-1]
+    ERR_BIT_TRACK = 32u,        // track length outside [-1, n] or bad track slot
 };
 
 constexpr int kHeadDim = 128;
+constexpr int kChunk = 128;     // tokens per chunk of the tensor-core extend
 
-// Recurrent (token-serial) kernels: decode, chain verify, and short extends.
-enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2, RECUR_TREE = 3 };
+// Recurrent (token-serial) kernels: decode, chain and tree verify, short extends, and the
+// within-chunk part of an extend's state-tracking snapshot.
+enum RecurMode : int {
+    RECUR_DECODE = 0,
+    RECUR_VERIFY = 1,
+    RECUR_EXTEND = 2,
+    RECUR_TREE = 3,
+    RECUR_TRACK = 4,
+};
 
 struct RecurParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -30,6 +39,8 @@ struct RecurParams {
     const uint8_t *prefix_mask;  // [B]   (extend)
     float *inter;                // [B][N][H][D][D] (verify)
     const int32_t *parents;      // [B][N] (tree verify)
+    const int32_t *track_lens;   // [B] (state tracking)
+    const int32_t *track_idx;    // [B] (state tracking)
     __nv_bfloat16 *out;
     unsigned int *err;           // device error word
     int B, H, N, T, num_slots;
@@ -72,6 +83,12 @@ struct ExtendParams {
     int nblk;      // blocks per request kept in the workspace
     float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
+    // State tracking (both null: none).  For b with track_lens[b] >= 0 the state after the first
+    // track_lens[b] tokens of the request is also written to slot track_idx[b]: this kernel
+    // stores the state at the chunk boundary at or before that token (the final state when it
+    // is the request's end), and RECUR_TRACK then advances the slot over the rest of the chunk.
+    const int32_t *track_lens;
+    const int32_t *track_idx;
 };
 
 // Split plan for a batch, from its shape and the device's SM count (seg_len == 0: no split).

@@ -47,6 +47,9 @@ class Workload:
     pool_fill: torch.Tensor | None = None    # fp32 [num_slots, H, D, D] when random_pool
     decode_steps: list = field(default_factory=list)  # tiny workload: [(q, k, v)] per step
     parents: torch.Tensor | None = None      # int32 [B, N] (tree verify)
+    track_lens: torch.Tensor | None = None   # int32 [B] (extend with state tracking)
+    track_idx: torch.Tensor | None = None    # int32 [B] (extend with state tracking)
+    accept_idx: torch.Tensor | None = None   # int32 [B] (verify followed by the commit)
 
     @property
     def B(self) -> int:
@@ -182,6 +185,32 @@ def verify_tree(seed: int = 0, B: int = 128, H: int = 64, parents=EAGLE_TREE8,
     return w
 
 
+def varlen_extend_tracked(seed: int = 0) -> Workload:
+    """The varlen extend workload with a state-tracking snapshot per request: track lengths
+    uniform in [0, length], track slots drawn from the slots no request uses.  The extra draws
+    come from a second generator (seed + 1000), so the base workload is unchanged."""
+    w = varlen_extend(seed)
+    g = torch.Generator().manual_seed(seed + 1000)
+    lens = (w.cu_seqlens[1:] - w.cu_seqlens[:-1]).tolist()
+    w.track_lens = torch.tensor([int(torch.randint(0, n + 1, (1,), generator=g)) for n in lens],
+                                dtype=torch.int32)
+    used = set(w.state_idx.tolist())
+    free = torch.tensor([s for s in range(w.num_slots) if s not in used], dtype=torch.int32)
+    w.track_idx = free[torch.randperm(len(free), generator=g)[:w.B]]
+    w.name = "varlen_extend_tracked_b8_h16"
+    return w
+
+
+def verify_commit(seed: int = 0) -> Workload:
+    """The chain-verify workload followed by the accepted-state commit: accept indices uniform
+    in [-1, N-1] (second generator, seed + 1000)."""
+    w = verify_chain(seed)
+    g = torch.Generator().manual_seed(seed + 1000)
+    w.accept_idx = torch.randint(-1, w.N, (w.B,), generator=g, dtype=torch.int32)
+    w.name = f"verify_commit_b{w.B}_n{w.N}_h{w.H}"
+    return w
+
+
 def custom_extend(lengths, H: int = 2, D: int = HEAD_DIM, layer_id: int = 0, L: int = 1,
                   prefix=None, num_slots: int | None = None, seed: int = 0,
                   shuffle_slots: bool = True) -> Workload:
@@ -229,4 +258,6 @@ WORKLOADS = {
     "long_prefill": long_prefill,
     "verify": verify_chain,
     "verify_tree": verify_tree,
+    "varlen_extend_tracked": varlen_extend_tracked,
+    "verify_commit": verify_commit,
 }
