@@ -278,10 +278,9 @@ class GpuCase:
                 self.kernel = "block_state_kernel + extend_chunked_kernel (one la_extend call)"
             self.track = None
             if w.track_lens is not None:
-                # one more launch: the within-chunk rest of each snapshot
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
-                self.launches_per_step += 1
-                self.kernel += " + recurrent_kernel<4> (state tracking)"
+                self.kernel = self.kernel.replace("extend_chunked_kernel",
+                                                  "extend_chunked_kernel<true>")
         if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
         if w.kind == "tree":

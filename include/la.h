@@ -56,8 +56,8 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,  /* valid but unsupported configuration (head_dim != 128, ...) */
     LA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     LA_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (reported by la_poll_error) */
-    LA_ERR_DEVICE_INPUT = 5  /* the device found a slot index out of range or inconsistent
-                                cu_seqlens (reported by la_poll_error) */
+    LA_ERR_DEVICE_INPUT = 5  /* the device found an index out of range: a slot, cu_seqlens, a tree
+                                parent, an accept or a track entry (reported by la_poll_error) */
 } la_status;
 
 typedef uint16_t la_bf16; /* bfloat16 bit pattern */
@@ -125,13 +125,14 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
  *                    or zero; its length: its final state); -1: no snapshot for b
  *   track_state_idx  device, int32 [B]: the pool slot that receives b's snapshot (ignored when
  *                    track_lens[b] == -1)
- * Both NULL: exactly la_extend.  One NULL: LA_ERR_INVALID.  Other arguments, outputs, the final
- * states and the errors are those of la_extend.  A track length outside [-1, length] or a track
+ * Both NULL: exactly la_extend.  One NULL: LA_ERR_INVALID.  Other arguments and errors are those
+ * of la_extend; outputs and final states equal la_extend's up to rounding (bit for bit for a
+ * request whose track length is -1, its length, or a multiple of 128).  A track length outside [-1, length] or a track
  * slot that is out of range or equal to the request's own slot skips that snapshot and is
  * reported by la_poll_error as LA_ERR_DEVICE_INPUT.  Track slots must differ from every slot the
  * call reads or writes otherwise and from one another (not checked: overlapping slots race).
- * Launches: la_extend's kernels, then one token-serial pass that advances each snapshot from the
- * chunk boundary before it (chunks are 128 tokens) to its token.
+ * Same launches as la_extend: the request's chunk grid is restarted at the tracked token, so the
+ * snapshot is the state the kernel carries at that chunk boundary (one more, partial, chunk).
  */
 la_status la_extend_tracked(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
                             const float *slopes, float *state_pool, int num_slots,

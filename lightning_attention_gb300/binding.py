@@ -235,11 +235,6 @@ def extend_noalloc(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_m
     _need(out, "out", torch.bfloat16, dev, (T, H * D))
     if max_seqlen is None:
         max_seqlen = T
-    if (track_lens is None) != (track_state_idx is None):
-        raise ValueError("track_lens and track_state_idx go together")
-    if track_lens is not None:
-        _need(track_lens, "track_lens", torch.int32, dev, (B,))
-        _need(track_state_idx, "track_state_idx", torch.int32, dev, (B,))
     with torch.cuda.device(dev):
         st = lib.la_extend_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                    num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),

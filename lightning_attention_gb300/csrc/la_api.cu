@@ -74,7 +74,8 @@ const char *la_status_string(la_status status) {
         case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch error";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device wait ran out";
         case LA_ERR_DEVICE_INPUT:
-            return "LA_ERR_DEVICE_INPUT: slot index out of range or inconsistent cu_seqlens";
+            return "LA_ERR_DEVICE_INPUT: a device-side index (slot, cu_seqlens, parent, accept "
+                   "or track entry) was out of range";
     }
     return "LA_ERR_UNKNOWN";
 }
@@ -284,25 +285,7 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
-    if (track_lens == nullptr) return launch_status(la::launch_extend_chunked(p, s));
-    if (la::launch_extend_chunked(p, s) != cudaSuccess) return LA_ERR_CUDA;
-    // the within-chunk rest of each snapshot, after the extend on the same stream
-    la::RecurParams r{};
-    r.k = p.k;
-    r.v = p.v;
-    r.q = p.q;
-    r.slopes = slopes;
-    r.pool = state_pool;
-    r.state_idx = state_idx;
-    r.cu_seqlens = cu_seqlens;
-    r.track_lens = track_lens;
-    r.track_idx = track_state_idx;
-    r.err = p.err;
-    r.B = B;
-    r.H = H;
-    r.T = T;
-    r.num_slots = num_slots;
-    return launch_status(la::launch_recurrent(la::RECUR_TRACK, r, s));
+    return launch_status(la::launch_extend_chunked(p, s));
 }
 
 }  // namespace

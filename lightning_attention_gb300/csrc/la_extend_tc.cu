@@ -14,7 +14,10 @@
 // exponentials (e^{-s i} / e^{-s j} overflows for s*C large).
 //
 // One CTA owns one (request b, head h, v-column block of DV = 64) and walks the request's chunks
-// of C = 128 tokens in order.  Roles (384 threads):
+// of C = 128 tokens in order.  A request with a state-tracking snapshot (same page, section
+// "额外覆盖": the state after its first track_len tokens also goes to a track slot) has its chunk
+// grid restarted at that token, so the snapshot is the state carried at a chunk boundary.
+// Roles (384 threads):
 //   warp 8      TMA producer: Q, K (C x 128) and the V block (C x 64) of each chunk into a
 //               two-stage ring (128-byte swizzled tiles, one mbarrier per stage);
 //   warps 10-11 convert each landed V tile to fp16 in place, off the epilogue's path;
@@ -62,7 +65,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int C = kChunk;           // chunk length in tokens
+constexpr int C = 128;              // chunk length in tokens
 constexpr int DV = 64;              // v columns per CTA
 constexpr int NV = kHeadDim / DV;   // v blocks per head
 constexpr int kEpiWarps = 8;
@@ -224,6 +227,7 @@ __device__ __forceinline__ void store_state_row(float *pool, int slot, int H, in
             make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
 }
 
+template <bool kTrack>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_chunked_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk,
@@ -289,7 +293,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool split = nseg_b > 1;
     const bool last_seg = g == nseg_b - 1;
     const int n = t1 - t0;
-    const int nchunks = (n + C - 1) / C;
+    // State tracking: the snapshot after the first tl tokens of the request is taken by the CTA
+    // whose segment holds token offset tl (the last segment when tl is the request's end).  That
+    // CTA restarts its chunk grid at the tracked token (local offset sp), so that a chunk ends
+    // exactly there, and stores the state it carries at that chunk boundary.  Every other CTA
+    // keeps the regular grid (sp = n + 1, past every chunk end).  Chunks are contiguous: chunk c
+    // starts where c - 1 ended and runs for min(C, bound - start) tokens, bound = sp before the
+    // tracked token and n after it.
+    int sp = n + 1;
+    if (kTrack) {
+        const int tl = p.track_lens[b];
+        const int tslot = p.track_idx[b];
+        if (tl >= 0) {
+            if (tl > n_req || tslot < 0 || tslot >= p.num_slots || tslot == slot) {
+                if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_TRACK);
+            } else {
+                const int tloc = tl - (t0 - t_req0);
+                if ((tloc >= 0 && tloc < n) || (tloc == n && last_seg)) sp = tloc;
+            }
+        }
+    }
+    const int nchunks = kTrack && sp <= n ? (sp + C - 1) / C + (n - sp + C - 1) / C
+                                          : (n + C - 1) / C;
     const uint64_t limit = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
@@ -329,13 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, ys = 0;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1;
                 if (c >= 2 &&
                     !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
                     break;
-                const int y = t0 + c * C;
+                const int y = t0 + (kTrack ? ys : c * C);
+                if (kTrack) ys += min(C, (ys < sp ? min(sp, n) : n) - ys);
                 const int xq = h * kHeadDim;
                 uint8_t *dst = sm + st * SZ_STAGE;
                 mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
@@ -476,24 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float *gstate =
             p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
-        // State tracking: the snapshot after the first tl tokens of the request starts as the
-        // state at request chunk boundary cb (tl rounded down to a chunk, or the request's end
-        // when tl is its length); the CTA whose segment holds that boundary stores it, as the
-        // state before its local chunk `snap`.  RECUR_TRACK adds the tokens between cb and tl.
-        int snap = -1, tslot = 0;
-        if (p.track_lens != nullptr) {
-            const int tl = p.track_lens[b];
-            tslot = p.track_idx[b];
-            if (tl >= 0) {
-                if (tl > n_req || tslot < 0 || tslot >= p.num_slots || tslot == slot) {
-                    if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_TRACK);
-                } else {
-                    const int cb = tl == n_req ? (n_req + C - 1) / C : tl / C;
-                    const int lc = cb - (t0 - t_req0) / C;
-                    if ((lc >= 0 && lc < nchunks) || (lc == nchunks && last_seg)) snap = lc;
-                }
-            }
-        }
         const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)wg * 32u;
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
@@ -544,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 32; ++x) S[x] = 0.f;
             }
-            if (snap == 0) store_state_row(p.pool, tslot, H, h, i, col0, S);
+            if (kTrack && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
             uint32_t w[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[x]);
@@ -553,6 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
         }
         fence_proxy_async_smem();
+        __shared__ int s_tslot;  // the track slot, read once per CTA at the snapshot
+        if (kTrack && threadIdx.x == 0) s_tslot = p.track_idx[b];
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables + P zeros
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_ready);
@@ -563,9 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool blk_b = q >= wg + 2;
         const size_t row_stride = (size_t)H * kHeadDim;
         bool ok = true;
+        int cs_next = 0;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
-            const int r = min(C, n - c * C);
+            // first token of the chunk and its length
+            const int cs = kTrack ? cs_next : c * C;
+            const int r = min(C, (kTrack && cs < sp ? min(sp, n) : n) - cs);
+            if (kTrack) cs_next = cs + r;
 
             // ---- mask: P = A o Dm D^-0.5 (fp16); K row half -> lambda K (fp16)
             if (!(ok = warp_wait_bar(&bars->a_full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
@@ -627,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st32(t_s, w);
                 store_state_split(s_hi, s_lo, i, wg, S);
-                if (c + 1 == snap) store_state_row(p.pool, tslot, H, h, i, col0, S);
+                if (kTrack && cs + r == sp)
+                    store_state_row(p.pool, s_tslot, H, h, i, col0, S);
                 tmem_st_wait();
             }
             fence_proxy_async_smem();
@@ -701,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     const int row = rbase + k;
                     if (row < r) {
-                        __nv_bfloat16 *dst = p.out + (size_t)(t0 + c * C + row) * row_stride +
+                        __nv_bfloat16 *dst = p.out + (size_t)(t0 + cs + row) * row_stride +
                                              (size_t)h * kHeadDim + col0 + pq * 8;
                         *reinterpret_cast<uint4 *>(dst) = ch[k];
                     }
@@ -791,13 +806,21 @@ cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream) {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!configured[dev]) {
-            e = cudaFuncSetAttribute(extend_chunked_kernel,
+            e = cudaFuncSetAttribute(extend_chunked_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(extend_chunked_kernel<true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
     }
-    extend_chunked_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    // the state-tracking variant only where snapshots are asked for: the plain path keeps its
+    // regular chunk grid and register budget
+    if (p.track_lens != nullptr)
+        extend_chunked_kernel<true><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    else
+        extend_chunked_kernel<false><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

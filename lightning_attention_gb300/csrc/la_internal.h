@@ -18,17 +18,9 @@ enum : unsigned int {
 };
 
 constexpr int kHeadDim = 128;
-constexpr int kChunk = 128;     // tokens per chunk of the tensor-core extend
 
-// Recurrent (token-serial) kernels: decode, chain and tree verify, short extends, and the
-// within-chunk part of an extend's state-tracking snapshot.
-enum RecurMode : int {
-    RECUR_DECODE = 0,
-    RECUR_VERIFY = 1,
-    RECUR_EXTEND = 2,
-    RECUR_TREE = 3,
-    RECUR_TRACK = 4,
-};
+// Recurrent (token-serial) kernels: decode, chain and tree verify, short extends.
+enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2, RECUR_TREE = 3 };
 
 struct RecurParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -39,8 +31,6 @@ struct RecurParams {
     const uint8_t *prefix_mask;  // [B]   (extend)
     float *inter;                // [B][N][H][D][D] (verify)
     const int32_t *parents;      // [B][N] (tree verify)
-    const int32_t *track_lens;   // [B] (state tracking)
-    const int32_t *track_idx;    // [B] (state tracking)
     __nv_bfloat16 *out;
     unsigned int *err;           // device error word
     int B, H, N, T, num_slots;
@@ -84,9 +74,8 @@ struct ExtendParams {
     float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
     // State tracking (both null: none).  For b with track_lens[b] >= 0 the state after the first
-    // track_lens[b] tokens of the request is also written to slot track_idx[b]: this kernel
-    // stores the state at the chunk boundary at or before that token (the final state when it
-    // is the request's end), and RECUR_TRACK then advances the slot over the rest of the chunk.
+    // track_lens[b] tokens of the request is also written to slot track_idx[b]; the CTA that
+    // holds that token restarts its chunk grid there and stores the state at that boundary.
     const int32_t *track_lens;
     const int32_t *track_idx;
 };

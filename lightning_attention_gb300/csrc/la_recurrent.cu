@@ -49,31 +49,16 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
 
     __shared__ __align__(16) float red[2][kWarps][kHeadDim];
 
-    int slot = p.state_idx[b];
+    const int slot = p.state_idx[b];
     if (slot < 0 || slot >= p.num_slots) {
         if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
         return;
     }
+    float *state = p.pool + ((size_t)slot * H + h) * (size_t)(kHeadDim * kHeadDim);
 
     int t_begin, n;
     bool from_pool = true;
-    if (MODE == RECUR_TRACK) {
-        // Rest of a state-tracking snapshot: the extend kernel left in the track slot the state
-        // at the chunk boundary before token track_len (and nothing to do when track_len is on
-        // a boundary or is the request's end); advance it over the tokens in between.  Invalid
-        // entries were reported by the extend kernel and are skipped here.
-        const int tl = p.track_lens[b];
-        const int t_req0 = p.cu_seqlens[b];
-        const int n_req = p.cu_seqlens[b + 1] - t_req0;
-        const int tslot = p.track_idx[b];
-        if (tl < 0 || t_req0 < 0 || n_req < 0 || t_req0 + n_req > p.T || tl >= n_req ||
-            tslot < 0 || tslot >= p.num_slots || tslot == slot)
-            return;
-        n = tl % kChunk;
-        if (n == 0) return;
-        t_begin = t_req0 + tl - n;
-        slot = tslot;
-    } else if (MODE == RECUR_EXTEND) {
+    if (MODE == RECUR_EXTEND) {
         t_begin = p.cu_seqlens[b];
         const int t_end = p.cu_seqlens[b + 1];
         if (t_begin < 0 || t_end < t_begin || t_end > p.T) {
@@ -102,7 +87,6 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
         }
     }
 
-    float *state = p.pool + ((size_t)slot * H + h) * (size_t)(kHeadDim * kHeadDim);
     float4 s[kRowsPerWarp];
     if (from_pool) {
 #pragma unroll
@@ -166,7 +150,6 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
             for (int r = 0; r < kRowsPerWarp; ++r)
                 __stcs(reinterpret_cast<float4 *>(dst + (size_t)(row0 + r) * kHeadDim + col), s[r]);
         }
-        if (MODE == RECUR_TRACK) continue;  // state only: the outputs are the extend's
         float(*buf)[kHeadDim] = red[t & 1];
         *reinterpret_cast<float4 *>(&buf[warp][col]) = o;
         __syncthreads();
@@ -239,7 +222,6 @@ cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t 
         case RECUR_VERIFY: recurrent_kernel<RECUR_VERIFY><<<grid, block, 0, stream>>>(p); break;
         case RECUR_EXTEND: recurrent_kernel<RECUR_EXTEND><<<grid, block, 0, stream>>>(p); break;
         case RECUR_TREE: recurrent_kernel<RECUR_TREE><<<grid, block, 0, stream>>>(p); break;
-        case RECUR_TRACK: recurrent_kernel<RECUR_TRACK><<<grid, block, 0, stream>>>(p); break;
     }
     return cudaGetLastError();
 }
