@@ -116,31 +116,46 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
                     la_stream stream);
 
 /*
- * la_extend_tracked -- la_extend plus a state-tracking snapshot per request ([LA-page §额外覆盖],
- * the extra-buffer state tracking of a prefill: at the track_len-th token the running state is
- * copied into a track slot, while the request's own slot still receives the final state and no
- * other slot is written).
+ * la_extend_ex -- la_extend with two options: a state-tracking snapshot per request, and the
+ * layout of out.
+ *
+ * State tracking ([LA-page §额外覆盖], the extra-buffer state tracking of a prefill: at the
+ * track_len-th token the running state is copied into a track slot, while the request's own slot
+ * still receives the final state and no other slot is written):
  *   track_lens       device, int32 [B]: the snapshot is the state after the first track_lens[b]
  *                    tokens of request b in this call (0: its initial state -- the prefix state
  *                    or zero; its length: its final state); -1: no snapshot for b
  *   track_state_idx  device, int32 [B]: the pool slot that receives b's snapshot (ignored when
  *                    track_lens[b] == -1)
- * Both NULL: exactly la_extend.  One NULL: LA_ERR_INVALID.  Other arguments and errors are those
- * of la_extend; outputs and final states equal la_extend's up to rounding (bit for bit for a
- * request whose track length is -1, its length, or a multiple of 128).  A track length outside [-1, length] or a track
- * slot that is out of range or equal to the request's own slot skips that snapshot and is
+ * Both NULL: no snapshots.  One NULL: LA_ERR_INVALID.  A track length outside [-1, length] or a
+ * track slot that is out of range or equal to the request's own slot skips that snapshot and is
  * reported by la_poll_error as LA_ERR_DEVICE_INPUT.  Track slots must differ from every slot the
- * call reads or writes otherwise and from one another (not checked: overlapping slots race).
- * Same launches as la_extend: the request's chunk grid is restarted at the tracked token, so the
- * snapshot is the state the kernel carries at that chunk boundary (one more, partial, chunk).
+ * call reads or writes otherwise and from one another (not checked: overlapping slots race).  The
+ * request's chunk grid is restarted at the tracked token, so the snapshot is the state the
+ * kernel carries at that chunk boundary (one more, partial, chunk); outputs and final states
+ * equal la_extend's up to rounding, bit for bit for a request whose track length is -1, its
+ * length, or a multiple of 128.
+ *
+ * Output layout ([LA-page §生产环境不支持, item 4]: the backend returns out flattened to
+ * [T, H*D] while the piecewise-CUDA-graph path writes a per-head [T, H, D] buffer; this lets out
+ * be any such buffer, including a strided view):
+ *   out_row_stride   elements from token t to token t+1 in out (0: H*D, the packed layout)
+ *   out_head_stride  elements from head h to head h+1 in out (0: D)
+ * Element j of head h of token t goes to out[t * out_row_stride + h * out_head_stride + j].  Both
+ * strides must be multiples of 8 (16-byte aligned stores), and rows of heads or heads of rows must
+ * not overlap (out_row_stride >= (H-1) * out_head_stride + D, or out_head_stride >=
+ * (T-1) * out_row_stride + D); LA_ERR_INVALID otherwise.  Elements between the written ones are
+ * left untouched.  A contiguous [T, H, D] buffer is the packed layout.
+ *
+ * All other arguments, the launches and the errors are those of la_extend.  With no snapshots and
+ * the packed layout this is la_extend.
  */
-la_status la_extend_tracked(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
-                            const float *slopes, float *state_pool, int num_slots,
-                            const int32_t *state_idx, const int32_t *cu_seqlens,
-                            const uint8_t *prefix_mask, const int32_t *track_lens,
-                            const int32_t *track_state_idx, la_bf16 *out, int B, int T, int H,
-                            int D, int max_seqlen, void *workspace, size_t workspace_bytes,
-                            la_stream stream);
+la_status la_extend_ex(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                       float *state_pool, int num_slots, const int32_t *state_idx,
+                       const int32_t *cu_seqlens, const uint8_t *prefix_mask,
+                       const int32_t *track_lens, const int32_t *track_state_idx, la_bf16 *out,
+                       int64_t out_row_stride, int64_t out_head_stride, int B, int T, int H, int D,
+                       int max_seqlen, void *workspace, size_t workspace_bytes, la_stream stream);
 
 /*
  * la_extend_workspace_size -- bytes of device scratch la_extend would use for a batch of this

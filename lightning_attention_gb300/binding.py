@@ -23,8 +23,8 @@ _lib = None
 STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
           4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_INPUT"}
 
-EXPORTS = ("la_slopes", "la_extend", "la_extend_tracked", "la_extend_workspace_size", "la_decode", "la_verify_chain",
-           "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
+EXPORTS = ("la_slopes", "la_extend", "la_extend_ex", "la_extend_workspace_size", "la_decode",
+           "la_verify_chain", "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
            "la_set_wait_limit")
 
 
@@ -66,9 +66,10 @@ def load():
         lib.la_verify_chain.restype = ip
         lib.la_verify_tree.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, vp]
         lib.la_verify_tree.restype = ip
-        lib.la_extend_tracked.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, vp, vp, ip, ip,
-                                          ip, ip, ip, vp, sz, vp]
-        lib.la_extend_tracked.restype = ip
+        i64 = ctypes.c_int64
+        lib.la_extend_ex.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, vp, vp, i64, i64, ip,
+                                     ip, ip, ip, ip, vp, sz, vp]
+        lib.la_extend_ex.restype = ip
         lib.la_commit_accepted.argtypes = [vp, vp, vp, ip, vp, ip, ip, ip, ip, vp]
         lib.la_commit_accepted.restype = ip
         lib.la_poll_error.argtypes = [vp]
@@ -106,6 +107,25 @@ def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _out_layout(out, dev, T: int, H: int, D: int):
+    """(row stride, head stride) in elements of an extend output: a [T, H*D] or [T, H, D] bf16
+    tensor whose innermost elements are contiguous (rows and heads may be strided)."""
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.bfloat16 or out.device != dev:
+        raise TypeError(f"out must be a bf16 tensor on {dev}")
+    if tuple(out.shape) == (T, H * D):
+        if out.stride(1) != 1:
+            raise ValueError("out rows must be contiguous")
+        return (out.stride(0) if T > 1 else H * D), D
+    if tuple(out.shape) == (T, H, D):
+        if out.stride(2) != 1:
+            raise ValueError("out heads must be contiguous")
+        # a stride of a dimension of size 1 is arbitrary in torch: give it a valid value
+        hs = out.stride(1) if H > 1 else D
+        rs = out.stride(0) if T > 1 else ((H - 1) * hs + D + 7) // 8 * 8
+        return rs, hs
+    raise ValueError(f"out must have shape {(T, H * D)} or {(T, H, D)}, got {tuple(out.shape)}")
 
 
 def slopes(H: int, layer_id: int, L: int) -> torch.Tensor:
@@ -149,7 +169,11 @@ def _cached_workspace(dev: torch.device, nbytes: int) -> torch.Tensor:
 def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
            max_seqlen: int | None = None, workspace=None, track_lens=None, track_state_idx=None):
     """Packed varlen extend (la_extend).  q, k, v: bf16 [T, H*D]; state_pool fp32
-    [S, H, D, D] updated in place; returns out bf16 [T, H*D].
+    [S, H, D, D] updated in place; returns out (allocated as bf16 [T, H*D] when not given).
+
+    out may be [T, H*D] or per-head [T, H, D], and a strided view (say a slice of a wider buffer,
+    or a head-major [H, T, D] buffer transposed): any layout other than the packed one goes
+    through la_extend_ex with its strides.
 
     workspace: None lets the binding supply the scratch la_extend_workspace_size asks for (a
     cached per-device buffer); False runs without scratch (no sequence split); a uint8 CUDA
@@ -157,7 +181,7 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     (or make one eager call of the same shape first), so that nothing is allocated.
 
     track_lens, track_state_idx: int32 [B] device tensors (both or neither) select
-    la_extend_tracked: the state after the first track_lens[b] tokens of request b is also
+    la_extend_ex's state tracking: the state after the first track_lens[b] tokens of request b is also
     written to slot track_state_idx[b] (-1: no snapshot)."""
     dev = q.device
     T = q.shape[0]
@@ -172,7 +196,7 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     _need(prefix_mask, "prefix_mask", torch.uint8, dev, (B,))
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, dev, (T, H * D))
+    rs, hs = _out_layout(out, dev, T, H, D)
     if max_seqlen is None:
         max_seqlen = T
     if (track_lens is None) != (track_state_idx is None):
@@ -191,18 +215,19 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
             _need(ws, "workspace", torch.uint8, dev)
         ws_ptr = _ptr(ws)
         ws_bytes = ws.numel() if ws is not None else 0
-        if track_lens is None:
+        plain = track_lens is None and (rs, hs) == (H * D, D)
+        if plain:
             st = load().la_extend(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                   num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),
                                   _ptr(out), B, T, H, D, int(max_seqlen), ws_ptr, ws_bytes,
                                   _stream_handle(dev))
         else:
-            st = load().la_extend_tracked(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_),
-                                          _ptr(state_pool), num_slots, _ptr(state_idx),
-                                          _ptr(cu_seqlens), _ptr(prefix_mask), _ptr(track_lens),
-                                          _ptr(track_state_idx), _ptr(out), B, T, H, D,
-                                          int(max_seqlen), ws_ptr, ws_bytes, _stream_handle(dev))
-    _check("la_extend" if track_lens is None else "la_extend_tracked", st)
+            st = load().la_extend_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                     num_slots, _ptr(state_idx), _ptr(cu_seqlens),
+                                     _ptr(prefix_mask), _ptr(track_lens), _ptr(track_state_idx),
+                                     _ptr(out), rs, hs, B, T, H, D, int(max_seqlen), ws_ptr,
+                                     ws_bytes, _stream_handle(dev))
+    _check("la_extend" if plain else "la_extend_ex", st)
     return out
 
 

@@ -229,11 +229,21 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
                       float *state_pool, int num_slots, const int32_t *state_idx,
                       const int32_t *cu_seqlens, const uint8_t *prefix_mask,
                       const int32_t *track_lens, const int32_t *track_state_idx, la_bf16 *out,
-                      int B, int T, int H, int D, int max_seqlen, void *workspace,
-                      size_t workspace_bytes, la_stream stream) {
+                      long long out_rs, long long out_hs, int B, int T, int H, int D,
+                      int max_seqlen, void *workspace, size_t workspace_bytes, la_stream stream) {
     if (B < 0 || T < 0 || H < 1 || D < 1 || num_slots < 1 || max_seqlen < 0)
         return LA_ERR_INVALID;
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    // output layout: 16-byte aligned rows and heads that do not overlap (rows of heads, or heads
+    // of rows), all inside the 2^40-element range the kernels index
+    if (out_rs == 0) out_rs = (long long)H * D;
+    if (out_hs == 0) out_hs = D;
+    if (out_rs < 0 || out_hs < 0 || out_rs % 8 != 0 || out_hs % 8 != 0) return LA_ERR_INVALID;
+    if (out_rs < (long long)(H - 1) * out_hs + D && out_hs < (long long)(T > 0 ? T - 1 : 0) * out_rs + D)
+        return LA_ERR_INVALID;
+    if (out_rs >= (1ll << 40) || out_hs >= (1ll << 40) ||
+        (long long)(T > 0 ? T - 1 : 0) * out_rs + (long long)(H - 1) * out_hs + D >= (1ll << 40))
+        return LA_ERR_UNSUPPORTED;
     if (B == 0) return LA_OK;
     if (!slopes || !state_pool || !state_idx || !cu_seqlens || !prefix_mask) return LA_ERR_INVALID;
     if (T > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID;
@@ -268,6 +278,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     p.lpt = (B > 1 && B <= 256) ? 1 : 0;
     p.track_lens = track_lens;
     p.track_idx = track_state_idx;
+    p.out_rs = out_rs;
+    p.out_hs = out_hs;
     if (workspace != nullptr && aligned16(workspace) && T > 0) {
         int sms = 0;
         if ((st = num_sms(&sms)) != LA_OK) return st;
@@ -298,20 +310,20 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
                     int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
                     la_stream stream) {
     return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
-                       nullptr, nullptr, out, B, T, H, D, max_seqlen, workspace, workspace_bytes,
-                       stream);
+                       nullptr, nullptr, out, 0, 0, B, T, H, D, max_seqlen, workspace,
+                       workspace_bytes, stream);
 }
 
-la_status la_extend_tracked(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
-                            const float *slopes, float *state_pool, int num_slots,
-                            const int32_t *state_idx, const int32_t *cu_seqlens,
-                            const uint8_t *prefix_mask, const int32_t *track_lens,
-                            const int32_t *track_state_idx, la_bf16 *out, int B, int T, int H,
-                            int D, int max_seqlen, void *workspace, size_t workspace_bytes,
-                            la_stream stream) {
+la_status la_extend_ex(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                       float *state_pool, int num_slots, const int32_t *state_idx,
+                       const int32_t *cu_seqlens, const uint8_t *prefix_mask,
+                       const int32_t *track_lens, const int32_t *track_state_idx, la_bf16 *out,
+                       int64_t out_row_stride, int64_t out_head_stride, int B, int T, int H, int D,
+                       int max_seqlen, void *workspace, size_t workspace_bytes, la_stream stream) {
     if ((track_lens == nullptr) != (track_state_idx == nullptr)) return LA_ERR_INVALID;
     return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
-                       track_lens, track_state_idx, out, B, T, H, D, max_seqlen, workspace,
+                       track_lens, track_state_idx, out, (long long)out_row_stride,
+                       (long long)out_head_stride, B, T, H, D, max_seqlen, workspace,
                        workspace_bytes, stream);
 }
 

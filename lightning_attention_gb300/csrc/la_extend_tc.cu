@@ -227,7 +227,8 @@ __device__ __forceinline__ void store_state_row(float *pool, int slot, int H, in
             make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
 }
 
-template <bool kTrack>
+// kEx: the options variant (state-tracking snapshots, caller-given output strides)
+template <bool kEx>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_chunked_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk,
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // starts where c - 1 ended and runs for min(C, bound - start) tokens, bound = sp before the
     // tracked token and n after it.
     int sp = n + 1;
-    if (kTrack) {
+    if (kEx && p.track_lens != nullptr) {
         const int tl = p.track_lens[b];
         const int tslot = p.track_idx[b];
         if (tl >= 0) {
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    const int nchunks = kTrack && sp <= n ? (sp + C - 1) / C + (n - sp + C - 1) / C
+    const int nchunks = kEx && sp <= n ? (sp + C - 1) / C + (n - sp + C - 1) / C
                                           : (n + C - 1) / C;
     const uint64_t limit = p.wait_limit_ns;
 
@@ -360,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c >= 2 &&
                     !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
                     break;
-                const int y = t0 + (kTrack ? ys : c * C);
-                if (kTrack) ys += min(C, (ys < sp ? min(sp, n) : n) - ys);
+                const int y = t0 + (kEx ? ys : c * C);
+                if (kEx) ys += min(C, (ys < sp ? min(sp, n) : n) - ys);
                 const int xq = h * kHeadDim;
                 uint8_t *dst = sm + st * SZ_STAGE;
                 mbar_arrive_expect_tx(&bars->full[st], kStageTxBytes);
@@ -552,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 32; ++x) S[x] = 0.f;
             }
-            if (kTrack && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
+            if (kEx && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
             uint32_t w[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[x]);
@@ -562,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __shared__ int s_tslot;  // the track slot, read once per CTA at the snapshot
-        if (kTrack && threadIdx.x == 0) s_tslot = p.track_idx[b];
+        if (kEx && threadIdx.x == 0 && p.track_lens != nullptr) s_tslot = p.track_idx[b];
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables + P zeros
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_ready);
@@ -571,15 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // below the diagonal (block cb > q is all zero and never written).
         const bool blk_a = q >= wg;
         const bool blk_b = q >= wg + 2;
-        const size_t row_stride = (size_t)H * kHeadDim;
+        // output layout: packed [T][H*128] unless the options variant was given other strides
+        const size_t row_stride = kEx ? (size_t)p.out_rs : (size_t)H * kHeadDim;
+        const size_t head_stride = kEx ? (size_t)p.out_hs : (size_t)kHeadDim;
         bool ok = true;
         int cs_next = 0;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
             // first token of the chunk and its length
-            const int cs = kTrack ? cs_next : c * C;
-            const int r = min(C, (kTrack && cs < sp ? min(sp, n) : n) - cs);
-            if (kTrack) cs_next = cs + r;
+            const int cs = kEx ? cs_next : c * C;
+            const int r = min(C, (kEx && cs < sp ? min(sp, n) : n) - cs);
+            if (kEx) cs_next = cs + r;
 
             // ---- mask: P = A o Dm D^-0.5 (fp16); K row half -> lambda K (fp16)
             if (!(ok = warp_wait_bar(&bars->a_full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
@@ -641,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st32(t_s, w);
                 store_state_split(s_hi, s_lo, i, wg, S);
-                if (kTrack && cs + r == sp)
+                if (kEx && cs + r == sp)
                     store_state_row(p.pool, s_tslot, H, h, i, col0, S);
                 tmem_st_wait();
             }
@@ -717,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int row = rbase + k;
                     if (row < r) {
                         __nv_bfloat16 *dst = p.out + (size_t)(t0 + cs + row) * row_stride +
-                                             (size_t)h * kHeadDim + col0 + pq * 8;
+                                             (size_t)h * head_stride + col0 + pq * 8;
                         *reinterpret_cast<uint4 *>(dst) = ch[k];
                     }
                 }
@@ -815,9 +818,9 @@ cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream) {
             configured[dev] = true;
         }
     }
-    // the state-tracking variant only where snapshots are asked for: the plain path keeps its
-    // regular chunk grid and register budget
-    if (p.track_lens != nullptr)
+    // the options variant (snapshots, output strides) only where they are asked for: the plain
+    // path keeps its regular chunk grid and register budget
+    if (p.track_lens != nullptr || p.out_rs != (long long)p.H * kHeadDim || p.out_hs != kHeadDim)
         extend_chunked_kernel<true><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     else
         extend_chunked_kernel<false><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);

@@ -78,6 +78,9 @@ struct ExtendParams {
     // holds that token restarts its chunk grid there and stores the state at that boundary.
     const int32_t *track_lens;
     const int32_t *track_idx;
+    // Output layout: element (t, h, j) of out is at t * out_rs + h * out_hs + j (elements); the
+    // packed [T][H*D] layout is out_rs = H*D, out_hs = D.
+    long long out_rs, out_hs;
 };
 
 // Split plan for a batch, from its shape and the device's SM count (seg_len == 0: no split).

@@ -84,13 +84,19 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.la_extend(n, n, n, n, n, 1, n, n, n, n, 0, 0, 1, 128, 0, n, 0, n) == 0
     assert lib.la_decode(n, n, n, n, n, 1, n, n, 0, 1, 128, n) == 0
     assert lib.la_verify_chain(n, n, n, n, n, 1, n, n, n, 0, 1, 1, 128, n) == 0
-    # tracked extend: the two track arrays go together; otherwise la_extend's checks
+    # extend with options: the two track arrays go together; output strides must be multiples
+    # of 8 that keep heads and rows apart; otherwise la_extend's checks
     ext = (n, n, n, n, n, 1, n, n, n)
-    assert lib.la_extend_tracked(*ext, n, n, n, 1, 1, 1, 64, 1, n, 0, n) == 2
-    assert lib.la_extend_tracked(*ext, n, n, n, 0, 0, 1, 128, 0, n, 0, n) == 0
+    assert lib.la_extend_ex(*ext, n, n, n, 0, 0, 1, 1, 1, 64, 1, n, 0, n) == 2
+    assert lib.la_extend_ex(*ext, n, n, n, 0, 0, 0, 0, 1, 128, 0, n, 0, n) == 0
     one = ct.c_void_p(16)
-    assert lib.la_extend_tracked(*ext, one, n, n, 0, 0, 1, 128, 0, n, 0, n) == 1
-    assert lib.la_extend_tracked(*ext, n, one, n, 0, 0, 1, 128, 0, n, 0, n) == 1
+    assert lib.la_extend_ex(*ext, one, n, n, 0, 0, 0, 0, 1, 128, 0, n, 0, n) == 1
+    assert lib.la_extend_ex(*ext, n, one, n, 0, 0, 0, 0, 1, 128, 0, n, 0, n) == 1
+    assert lib.la_extend_ex(*ext, n, n, n, 260, 0, 0, 0, 2, 128, 0, n, 0, n) == 1  # not x8
+    assert lib.la_extend_ex(*ext, n, n, n, 128, 128, 0, 4, 2, 128, 0, n, 0, n) == 1  # overlap
+    assert lib.la_extend_ex(*ext, n, n, n, -8, 0, 0, 0, 2, 128, 0, n, 0, n) == 1
+    assert lib.la_extend_ex(*ext, n, n, n, 128, 512, 0, 4, 2, 128, 0, n, 0, n) == 0  # head-major
+    assert lib.la_extend_ex(*ext, n, n, n, 384, 128, 0, 4, 2, 128, 0, n, 0, n) == 0  # wide rows
     # accepted-state commit: same rules
     assert lib.la_commit_accepted(n, n, n, 1, n, 1, 1, 1, 64, n) == 2
     assert lib.la_commit_accepted(n, n, n, 1, n, 1, 0, 1, 128, n) == 1

@@ -1,4 +1,4 @@
-"""GPU parity of prefill state tracking (la_extend_tracked) against the fp64 oracle.
+"""GPU parity of prefill state tracking (la_extend_ex) against the fp64 oracle.
 
 The page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析" (section
 "额外覆盖：mamba 状态跟踪与布局鲁棒性") describes the check: at the track_len-th token the running
