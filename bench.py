@@ -50,19 +50,19 @@ FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCE = {
     "decode": "la_recurrent.cu",
     "verify": "la_recurrent.cu",
-    "varlen_extend": "la_extend_tc.cu",
-    "long_prefill": "la_extend_tc.cu",
+    "varlen_extend": "la_extend_w.cu",
+    "long_prefill": "la_extend_w.cu",
     "verify_tree": "la_recurrent.cu",
-    "varlen_extend_tracked": "la_extend_tc.cu",
+    "varlen_extend_tracked": "la_extend_w.cu",
     "verify_commit": "la_recurrent.cu",
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
     "verify": "recurrent_kernel<1>",
-    "varlen_extend": "extend_chunked_kernel",
-    "long_prefill": "extend_chunked_kernel",
+    "varlen_extend": "extend_wide_kernel",
+    "long_prefill": "extend_wide_kernel",
     "verify_tree": "recurrent_kernel<3>",
-    "varlen_extend_tracked": "extend_chunked_kernel",
+    "varlen_extend_tracked": "extend_wide_kernel",
     "verify_commit": "recurrent_kernel<1>",
 }
 # Small cases of the same kernels for multi-pass ncu captures (--profile-calls); a few GB at most.
@@ -275,12 +275,12 @@ class GpuCase:
             if la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen) > 0:
                 # long requests split into segments: block-state kernel, then the extend kernel
                 self.launches_per_step = 2
-                self.kernel = "block_state_kernel + extend_chunked_kernel (one la_extend call)"
+                self.kernel = "block_state_kernel + extend_wide_kernel (one la_extend call)"
             self.track = None
             if w.track_lens is not None:
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
-                self.kernel = self.kernel.replace("extend_chunked_kernel",
-                                                  "extend_chunked_kernel<true>")
+                self.kernel = self.kernel.replace("extend_wide_kernel",
+                                                  "extend_wide_kernel<true>")
         if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
         if w.kind == "tree":

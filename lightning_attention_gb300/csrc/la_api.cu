@@ -13,6 +13,10 @@
 
 namespace {
 
+// Extend kernel: 1 = one CTA per (request, head), every MMA 128 columns wide (la_extend_w.cu);
+// 2 = two CTAs per head, one per 64-column half of the values (la_extend_tc.cu).
+constexpr int kExtendCtasPerHead = 1;
+
 // Per-device error word: kernels OR bits into it when they find a fault the host cannot see
 // (out-of-range slot, inconsistent cu_seqlens, a bounded wait that ran out).  Module-scope
 // device variable; its address is looked up once per device and passed to kernels.
@@ -283,7 +287,7 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     if (workspace != nullptr && aligned16(workspace) && T > 0) {
         int sms = 0;
         if ((st = num_sms(&sms)) != LA_OK) return st;
-        const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms);
+        const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead);
         if (pl.seg_len > 0 && (unsigned long long)workspace_bytes >= pl.ws_bytes) {
             p.seg_len = pl.seg_len;
             p.blk_len = pl.blk_len;
@@ -297,7 +301,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
-    return launch_status(la::launch_extend_chunked(p, s));
+    return launch_status(kExtendCtasPerHead == 1 ? la::launch_extend_wide(p, s)
+                                                 : la::launch_extend_chunked(p, s));
 }
 
 }  // namespace
@@ -336,7 +341,7 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
     int sms = 0;
     la_status st = num_sms(&sms);
     if (st != LA_OK) return st;
-    *bytes = (size_t)la::plan_split(B, H, max_seqlen, sms).ws_bytes;
+    *bytes = (size_t)la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead).ws_bytes;
     return LA_OK;
 }
 

@@ -272,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // head) and u < num_sms / 2, cut each request into G = floor(num_sms / u) segments (at least
 // 8 chunks each), and each segment into P blocks so that the block-state kernel also fills the
 // GPU.  Workspace: B * H * (1 + nblk) fp32 D x D matrices.
-SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms) {
+SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_head) {
     SplitPlan pl{0, 0, 1, 0, 0ull};
-    const long long units = (long long)B * H * 2;
+    const long long units = (long long)B * H * ctas_per_head;
     if (B <= 0 || units <= 0 || num_sms <= 0 || 2 * units > num_sms) return pl;
     const int min_seg = 8 * C;
     int G = (int)(num_sms / units);

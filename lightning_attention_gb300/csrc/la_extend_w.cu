@@ -1,0 +1,818 @@
+// la_extend_w.cu -- chunked seg_la extend on the 5th-generation tensor cores, one CTA per
+// (request, head): every MMA is 128 columns wide and the masked score matrix P lives in tensor
+// memory.
+//
+// Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
+// "独立参考实现：逐 token 递推公式": per head, S_t = S_{t-1} e^{-s} + outer(k_t, v_t) and
+// o_t = (q_t @ S_t) D^-0.5, over each request's tokens, from the request's pool state (or zero),
+// final state written back.  A request with a state-tracking snapshot (same page, section
+// "额外覆盖") has its chunk grid restarted at the tracked token, so the snapshot is the state at a
+// chunk boundary.
+//
+// Chunked form (exact up to rounding; local token indices i, j in [0, r), S the state before the
+// chunk):
+//   o_i    = D^-0.5 gamma_i (Q S)_i  +  ((Q K^T o Dm) D^-0.5 V)_i,
+//            gamma_i = e^{-s (i+1)},  Dm_ij = e^{-s (i-j)} if j <= i, else 0
+//   S_next = e^{-s r} S  +  K^T diag(lambda) V,       lambda_j = e^{-s (r-1-j)}
+//
+// Why one CTA per head.  An M = 128 tcgen05.mma costs about the same whether N is 64 or 128, so
+// covering all 128 value columns in one CTA halves the MMA instructions per head and chunk, and
+// the score matrix Q K^T and its mask are built once per head instead of once per column half.
+// What it costs is storage: the value tile doubles, so Q has a single shared-memory buffer (K and
+// V keep two), P moves into tensor memory in place of Q K^T, and the state update accumulates
+// straight into the fp32 master state in tensor memory (pre-scaled by the next chunk's decay)
+// instead of into a separate U buffer.
+//
+// Roles (384 threads):
+//   warp 8      TMA producer: K and V of each chunk into a two-stage ring, Q into its buffer once
+//               the previous chunk's Q products are done;
+//   warps 10-11 convert each landed V tile (128 x 128) to fp16 in place;
+//   warp 9      TMEM allocator and MMA issuer (one thread), all accumulating in fp32:
+//                 MMA1  A       = Q K^T              bf16 x bf16  -> TMEM (128 columns)
+//                 MMA2  Oint    = Q S_hi + Q S_lo    bf16 x bf16  -> TMEM (128 columns)
+//                 MMA4  S      += (lambda K)^T V     fp16 x fp16  -> TMEM (the state itself)
+//                 MMA3  Ointra  = P V                fp16 (P from TMEM) x fp16
+//   warps 0-3   P: read A for their 32 rows, write P = A o Dm D^-0.5 as fp16 pairs over the first
+//               64 TMEM columns of A (every read of a row happens in the warp that overwrites it);
+//   warps 4-7   scale K by lambda into fp16 in place (both 64-column halves of their 32 rows);
+//   warps 0-7   then, per 64-column half (warp / 4): the state pass (S to bf16 hi + lo in shared
+//               memory for MMA2, snapshot if tracked, S times the next chunk's decay back to TMEM)
+//               and the output pass (gamma D^-0.5 Oint + Ointra -> bf16 -> global).
+// TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128.
+//
+// Per chunk c, the MMA thread issues MMA2_c (after the state pass of c-1 and the output pass of
+// c-1), MMA4_c (after K is scaled and V converted), MMA3_c (after P), then MMA1_{c+1}.  The
+// orders that make the buffer reuse safe: MMA1_{c+1} overwrites A/P after MMA3_c by issue order;
+// P_c is written after MMA1_c is complete; the state pass of c rewrites S_hi/S_lo after u_full(c),
+// which also covers MMA2_c; MMA4_c accumulates into S after the state pass of c-1 has scaled it;
+// Q_{c+1} is loaded after MMA2_c (and so MMA1_c) is complete.
+//
+// Every mbarrier wait is bounded (a globaltimer deadline).  A wait that runs out sets the error
+// word and an abort flag; every role then leaves its loop, the producer waits for its own copies
+// in flight and the MMA issuer for its MMAs, and the CTA frees its TMEM and exits.  No named
+// barrier is used after the first wait of the kernel.
+#include <cuda.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "la_internal.h"
+#include "la_sm100.cuh"
+
+namespace la {
+
+bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);  // la_extend_tc.cu
+
+namespace {
+
+using namespace sm100;
+
+constexpr int C = 128;              // chunk length in tokens
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kConvWarp0 = 10;      // warps 10, 11: V tile to fp16
+constexpr int kConvWarps = 2;
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_A = 0;        // 128 columns: Q K^T (fp32); P (fp16 pairs) in columns 0-63
+constexpr uint32_t TM_OI = 128;     // 128 columns: Q S
+constexpr uint32_t TM_OP = 256;     // 128 columns: P V
+constexpr uint32_t TM_S = 384;      // 128 columns: the fp32 master state
+// head_dim^-0.5 for head_dim = 128, i.e. 2^-3.5
+constexpr float kScale = 0.08838834764831845f;
+
+// Shared memory (offsets from a 1024-byte aligned base).  Every tile is [128][128] 16-bit values
+// as two 128-byte-swizzled [128][64] blocks 16 KiB apart.
+constexpr uint32_t SZ_T = C * kHeadDim * 2;         // 32 KiB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = SZ_T;                   // stage s: K at OFF_KV + s SZ_KV, V after it
+constexpr uint32_t SZ_KV = 2 * SZ_T;
+constexpr uint32_t OFF_SHI = OFF_KV + 2 * SZ_KV;
+constexpr uint32_t OFF_SLO = OFF_SHI + SZ_T;
+constexpr uint32_t OFF_TAB = OFF_SLO + SZ_T;        // e^{-s m}, m = 0..C
+constexpr uint32_t OFF_TABP = OFF_TAB + 544;        // e^{-s m} D^-0.5, m = 0..C
+constexpr uint32_t OFF_BAR = OFF_TABP + 544;
+constexpr uint32_t SZ_BAR = 256;
+constexpr uint32_t kSmemBytes = OFF_BAR + SZ_BAR + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(OFF_BAR % 8 == 0, "barrier alignment");
+static_assert(OFF_KV % 1024 == 0 && SZ_KV % 1024 == 0 && OFF_SHI % 1024 == 0 &&
+                  OFF_SLO % 1024 == 0,
+              "operand tiles start on 1024-byte swizzle atoms");
+
+struct Bars {
+    uint64_t q_full;      // TMA -> all: Q of the chunk loaded
+    uint64_t q_empty;     // MMA -> TMA: MMA1 and MMA2 of the chunk done with Q
+    uint64_t kv_full[2];  // TMA -> all: K, V of the chunk loaded
+    uint64_t kv_empty[2]; // MMA -> TMA: MMA3 and MMA4 of the chunk done with K and V
+    uint64_t a_full;      // MMA1 done
+    uint64_t v_ready[2];  // converter warps: V tile in fp16 (2 warp arrivals)
+    uint64_t k_ready;     // warps 4-7: K scaled by lambda into fp16 (4)
+    uint64_t p_ready;     // warps 0-3: P written to TMEM (4)
+    uint64_t s_ready;     // epilogue: S_hi/S_lo written, decayed S back in TMEM (8)
+    uint64_t o_free;      // epilogue: Oint/Ointra read (8)
+    uint64_t u_full;      // MMA4 done: S of the chunk complete (and, by issue order, MMA2)
+    uint64_t o_full;      // MMA3 done
+    uint64_t drain;       // MMA issuer: all MMAs done
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= SZ_BAR, "barrier block");
+
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                         volatile int *abort_flag, unsigned int *err) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_BIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// All 32 lanes wait (each acquires the barrier); the warp proceeds only if every lane succeeded.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort_flag, unsigned int *err) {
+    const bool ok = wait_bar(bar, parity, limit_ns, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Descriptor offsets (16-byte units) of the kk-th 16-deep slice of the contraction: K-major tiles
+// are two 64-column blocks 16 KiB apart, each slice 32 bytes into the 128-byte row; MN-major
+// tiles advance 16 rows (2 KiB) per slice.
+__device__ __forceinline__ uint64_t kofs(int kk) {
+    return (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+}
+__device__ __forceinline__ uint64_t mnofs(int kk) { return (uint64_t)(kk * 128); }
+
+// D[tmem] (+)= A[tmem] * B[smem], fp16 operands, fp32 accumulate; issued by one thread.  A is
+// M = 128 lanes by K = 16 values, two fp16 values per 32-bit column (even index in the low half).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-collective TMEM store of 16 consecutive 32-bit columns per lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// 16-byte chunk: 8 bf16 -> 8 fp16 times f.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x, float f) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 32 state columns (64 atom + 32 sub .. + 31) of row `row` as bf16 hi and lo into the [128][128]
+// MN-major operand tiles.
+__device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, int row, int atom,
+                                                  int sub, const float *S) {
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = S[k4 * 8 + 2 * e], b = S[k4 * 8 + 2 * e + 1];
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            const float2 hf = __bfloat1622float2(h);
+            hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+            lo[e] = pack_bf16x2(a - hf.x, b - hf.y);
+        }
+        const int off = atom * 16384 + row * 128 + (((sub * 4 + k4) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(s_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// P row segment: 32 columns of block cb of row i, decay-masked and scaled, as 16 fp16 pairs.
+// Below the diagonal block (cb < i / 32) every i - j >= 1, so no mask is needed; in the diagonal
+// block the table is read at a clamped index and the upper triangle selected away afterwards.
+__device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], const float *tabp,
+                                        uint32_t (&pk)[16]) {
+    const int d = i - cb * 32;  // i - j for jj = 0
+    if (d >= 32) {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2)
+            pk[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * tabp[d - jj],
+                                     __uint_as_float(v[jj + 1]) * tabp[d - jj - 1]);
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2) {
+            const int d0 = d - jj, d1 = d - jj - 1;
+            const float x0 = __uint_as_float(v[jj]) * tabp[max(d0, 0)];
+            const float x1 = __uint_as_float(v[jj + 1]) * tabp[max(d1, 0)];
+            pk[jj >> 1] = pack_f16x2(d0 >= 0 ? x0 : 0.f, d1 >= 0 ? x1 : 0.f);
+        }
+    }
+}
+
+// This thread's share of a state (row i, columns col0 .. col0 + 31) into pool slot `slot`.
+__device__ __forceinline__ void store_state_row(float *pool, int slot, int H, int h, int i,
+                                                int col0, const float *S) {
+    float *dst = pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col0;
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+        *reinterpret_cast<float4 *>(dst + 4 * x) =
+            make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+}
+
+// Length of the chunk that starts at local token cs, with the grid restarted at sp (n + 1: none).
+__device__ __forceinline__ int chunk_len(bool ex, int cs, int sp, int n) {
+    return min(C, (ex && cs < sp ? min(sp, n) : n) - cs);
+}
+
+// kEx: the options variant (state-tracking snapshots, caller-given output strides)
+template <bool kEx>
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_wide_kernel(const __grid_constant__ CUtensorMap tq,
+                       const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const ExtendParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+    float *tab = reinterpret_cast<float *>(sm + OFF_TAB);
+    float *tabp = reinterpret_cast<float *>(sm + OFF_TABP);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = p.H;
+    const int g = blockIdx.x % p.nseg;  // segment of the request (0 when not split)
+    const int bh = blockIdx.x / p.nseg;
+    const int h = bh % H;
+    int b = bh / H;
+    if (p.lpt) {
+        // Longest request first: CTAs are issued in index order, so taking requests in
+        // decreasing length order (ties by index) keeps long requests from finishing last.
+        __shared__ int s_req;
+        const int want = b;
+        for (int t = threadIdx.x; t < p.B; t += kThreads) {
+            const int lt = p.cu_seqlens[t + 1] - p.cu_seqlens[t];
+            int rank = 0;
+            for (int u = 0; u < p.B; ++u) {
+                const int lu = p.cu_seqlens[u + 1] - p.cu_seqlens[u];
+                rank += (lu > lt) || (lu == lt && u < t);
+            }
+            if (rank == want) s_req = t;
+        }
+        __syncthreads();
+        b = s_req;
+    }
+
+    // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
+    const int slot = p.state_idx[b];
+    const int t_req0 = p.cu_seqlens[b];
+    const int t_req1 = p.cu_seqlens[b + 1];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        return;
+    }
+    if (t_req0 < 0 || t_req1 < t_req0 || t_req1 > p.T) {
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
+        return;
+    }
+    // Segment [t0, t1) of the request: the whole request unless long requests are split.
+    const int n_req = t_req1 - t_req0;
+    int nseg_b = 1, t0 = t_req0, t1 = t_req1;
+    if (p.seg_len > 0) {
+        nseg_b = n_req > 0 ? (n_req + p.seg_len - 1) / p.seg_len : 1;
+        if (g >= nseg_b) return;
+        t0 = t_req0 + g * p.seg_len;
+        t1 = min(t_req1, t0 + p.seg_len);
+    }
+    const bool split = nseg_b > 1;
+    const bool last_seg = g == nseg_b - 1;
+    const int n = t1 - t0;
+    // State tracking: the CTA whose segment holds token offset tl (the last segment when tl is
+    // the request's end) restarts its chunk grid at that token (local offset sp) and stores the
+    // state it carries at that boundary; every other CTA keeps the regular grid (sp = n + 1).
+    int sp = n + 1;
+    if (kEx && p.track_lens != nullptr) {
+        const int tl = p.track_lens[b];
+        const int tslot = p.track_idx[b];
+        if (tl >= 0) {
+            if (tl > n_req || tslot < 0 || tslot >= p.num_slots || tslot == slot) {
+                if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_TRACK);
+            } else {
+                const int tloc = tl - (t0 - t_req0);
+                if ((tloc >= 0 && tloc < n) || (tloc == n && last_seg)) sp = tloc;
+            }
+        }
+    }
+    const int nchunks = kEx && sp <= n ? (sp + C - 1) / C + (n - sp + C - 1) / C
+                                       : (n + C - 1) / C;
+    const uint64_t limit = p.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->v_ready[s], kConvWarps);
+        }
+        mbar_init(&bars->a_full, 1);
+        mbar_init(&bars->k_ready, kEpiWarps / 2);
+        mbar_init(&bars->p_ready, kEpiWarps / 2);
+        mbar_init(&bars->s_ready, kEpiWarps);
+        mbar_init(&bars->o_free, kEpiWarps);
+        mbar_init(&bars->u_full, 1);
+        mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0 && nchunks > 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int *abort_flag = &bars->abort_flag;
+
+    const uint32_t s_base = smem_u32(sm);
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int kv_issued = 0, q_issued = 0, ys = 0;
+            const int xq = h * kHeadDim;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1;
+                const int y = t0 + (kEx ? ys : c * C);
+                if (kEx) ys += chunk_len(true, ys, sp, n);
+                if (c >= 2 &&
+                    !wait_bar(&bars->kv_empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                uint8_t *kv = sm + OFF_KV + st * SZ_KV;
+                mbar_arrive_expect_tx(&bars->kv_full[st], 2 * SZ_T);
+                tma_load_2d(kv, &tk, &bars->kv_full[st], xq, y);
+                tma_load_2d(kv + 16384, &tk, &bars->kv_full[st], xq + 64, y);
+                tma_load_2d(kv + SZ_T, &tv, &bars->kv_full[st], xq, y);
+                tma_load_2d(kv + SZ_T + 16384, &tv, &bars->kv_full[st], xq + 64, y);
+                kv_issued = c + 1;
+                if (c >= 1 && !wait_bar(&bars->q_empty, (c - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                mbar_arrive_expect_tx(&bars->q_full, SZ_T);
+                tma_load_2d(sm + OFF_Q, &tq, &bars->q_full, xq, y);
+                tma_load_2d(sm + OFF_Q + 16384, &tq, &bars->q_full, xq + 64, y);
+                q_issued = c + 1;
+            }
+            // Copies still in flight must land before the CTA's shared memory goes away.
+            int dummy = 0;
+            for (int c = (kv_issued >= 2 ? kv_issued - 2 : 0); c < kv_issued; ++c)
+                wait_bar(&bars->kv_full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
+            if (q_issued > 0)
+                wait_bar(&bars->q_full, (q_issued - 1) & 1, kDrainLimitNs, &dummy, p.err);
+        }
+    } else if (warp >= kConvWarp0) {
+        // ------------------------------------------------------------------ V tile to fp16
+        // Two warps convert each landed V tile in place (32 KiB, 16-byte chunks, 64 consecutive
+        // chunks per round), well before MMA4 and MMA3 need it.
+        const int cl = (warp - kConvWarp0) * 32 + lane;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1;
+            if (!warp_wait_bar(&bars->kv_full[st], (c >> 1) & 1, limit, abort_flag, p.err))
+                break;
+            uint4 *vt = reinterpret_cast<uint4 *>(sm + OFF_KV + st * SZ_KV + SZ_T);
+            constexpr int kRounds = (int)(SZ_T / 16 / (32 * kConvWarps));  // 32
+#pragma unroll
+            for (int m0 = 0; m0 < kRounds; m0 += 8) {
+                uint4 vbuf[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) vbuf[m] = vt[cl + 32 * kConvWarps * (m0 + m)];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    vt[cl + 32 * kConvWarps * (m0 + m)] = bf16x8_to_f16x8(vbuf[m], 1.f);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->v_ready[st]);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idA = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t idI = idesc_bf16_f32(128, 128, false, true);
+            const uint32_t idP = idesc_f16_f32(128, 128, false, true);
+            const uint32_t idU = idesc_f16_f32(128, 128, true, true);
+            const uint64_t dQ = sdesc_sw128(s_base + OFF_Q, 16, 1024);
+            const uint64_t dK0 = sdesc_sw128(s_base + OFF_KV, 16, 1024);
+            const uint64_t dKt0 = sdesc_sw128(s_base + OFF_KV, 16384, 1024);
+            const uint64_t dV0 = sdesc_sw128(s_base + OFF_KV + SZ_T, 16384, 1024);
+            const uint64_t stage_step = SZ_KV >> 4;
+            const uint64_t dHi = sdesc_sw128(s_base + OFF_SHI, 16384, 1024);
+            const uint64_t dLo = sdesc_sw128(s_base + OFF_SLO, 16384, 1024);
+            auto issue_qk = [&](int c) -> bool {
+                const int st = c & 1;
+                if (!wait_bar(&bars->q_full, c & 1, limit, abort_flag, p.err) ||
+                    !wait_bar(&bars->kv_full[st], (c >> 1) & 1, limit, abort_flag, p.err))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_A, dQ + kofs(kk), dK0 + st * stage_step + kofs(kk), idA,
+                             kk > 0);
+                mma_commit(&bars->a_full);
+                return true;
+            };
+            bool ok = true;
+            if (nchunks > 0) ok = issue_qk(0);
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int st = c & 1;
+                // Oint = Q S_{c-1}: needs the previous state and the previous outputs read
+                if (!wait_bar(&bars->s_ready, c & 1, limit, abort_flag, p.err) ||
+                    (c >= 1 && !wait_bar(&bars->o_free, (c - 1) & 1, limit, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_OI, dQ + kofs(kk), dHi + mnofs(kk), idI, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_OI, dQ + kofs(kk), dLo + mnofs(kk), idI, 1);
+                mma_commit(&bars->q_empty);
+                // S += (lambda K)^T V once K is scaled and V converted: it runs while P is built
+                if (!wait_bar(&bars->k_ready, c & 1, limit, abort_flag, p.err) ||
+                    !wait_bar(&bars->v_ready[st], (c >> 1) & 1, limit, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_S, dKt0 + st * stage_step + mnofs(kk),
+                             dV0 + st * stage_step + mnofs(kk), idU, 1);
+                mma_commit(&bars->u_full);
+                // Ointra = P V once P is in TMEM: it runs while the epilogue does the state pass
+                if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_tmem_a(tbase + TM_OP, tbase + TM_A + (uint32_t)(kk * 8),
+                                   dV0 + st * stage_step + mnofs(kk), idP, kk > 0);
+                mma_commit(&bars->o_full);
+                mma_commit(&bars->kv_empty[st]);
+                if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
+            }
+            // Every issued MMA must finish before TMEM is freed.
+            mma_commit(&bars->drain);
+            int dummy = 0;
+            wait_bar(&bars->drain, 0, kDrainLimitNs, &dummy, p.err);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue warps
+        const int q = warp & 3;            // TMEM lane quarter
+        const int wg = warp >> 2;          // 64-column half for the state and output passes
+        const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (S)
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+
+        const float slope = p.slopes[h];
+        for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
+            const float e = expf(-slope * (float)m);
+            tab[m] = e;
+            tabp[m] = e * kScale;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables
+        uint8_t *s_hi = sm + OFF_SHI;
+        uint8_t *s_lo = sm + OFF_SLO;
+        // this row's share of the pool state: columns 64 wg .. 64 wg + 63
+        float *gstate =
+            p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)(wg * 64);
+        {
+            const int r0 = nchunks > 0 ? chunk_len(kEx, 0, sp, n) : 0;
+            const float d0s = tab[r0];  // 1 when there is no chunk
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+                const int col0 = wg * 64 + sub * 32;
+                float S[32];
+                if (split) {
+                    // S = e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, from
+                    // the workspace the block-state kernel filled.
+                    const float *w0 = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) *
+                                                 (kHeadDim * kHeadDim) +
+                                      (size_t)i * kHeadDim + col0;
+                    const float d0 = expf(-slope * (float)g * (float)p.seg_len);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const float4 f = reinterpret_cast<const float4 *>(w0)[x];
+                        S[4 * x] = d0 * f.x;
+                        S[4 * x + 1] = d0 * f.y;
+                        S[4 * x + 2] = d0 * f.z;
+                        S[4 * x + 3] = d0 * f.w;
+                    }
+                    const int nb = g * (p.seg_len / p.blk_len);
+                    for (int kb = 0; kb < nb; ++kb) {
+                        const float dk =
+                            expf(-slope * (float)(g * p.seg_len - (kb + 1) * p.blk_len));
+                        const float4 *wk = reinterpret_cast<const float4 *>(
+                            w0 + (size_t)(1 + kb) * (kHeadDim * kHeadDim));
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            const float4 f = wk[x];
+                            S[4 * x] = fmaf(dk, f.x, S[4 * x]);
+                            S[4 * x + 1] = fmaf(dk, f.y, S[4 * x + 1]);
+                            S[4 * x + 2] = fmaf(dk, f.z, S[4 * x + 2]);
+                            S[4 * x + 3] = fmaf(dk, f.w, S[4 * x + 3]);
+                        }
+                    }
+                } else if (p.prefix_mask[b]) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const float4 f =
+                            *reinterpret_cast<const float4 *>(gstate + sub * 32 + 4 * x);
+                        S[4 * x] = f.x;
+                        S[4 * x + 1] = f.y;
+                        S[4 * x + 2] = f.z;
+                        S[4 * x + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) S[x] = 0.f;
+                }
+                if (kEx && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
+                store_state_split(s_hi, s_lo, i, wg, sub, S);
+                // TMEM holds e^{-s r_0} S_0, onto which MMA4 of chunk 0 accumulates
+                uint32_t w[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[x] * d0s);
+                tmem_st32(tbase + lane_off + TM_S + (uint32_t)col0, w);
+            }
+            tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_ready);
+
+        // output layout: packed [T][H*128] unless the options variant was given other strides
+        const size_t row_stride = kEx ? (size_t)p.out_rs : (size_t)H * kHeadDim;
+        const size_t head_stride = kEx ? (size_t)p.out_hs : (size_t)kHeadDim;
+        bool ok = true;
+        int cs_next = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1;
+            // first token of the chunk and its length
+            const int cs = kEx ? cs_next : c * C;
+            const int r = chunk_len(kEx, cs, sp, n);
+            if (kEx) cs_next = cs + r;
+
+            if (!(ok = warp_wait_bar(&bars->a_full, c & 1, limit, abort_flag, p.err))) break;
+            tc_fence_after();
+            if (wg == 1) {
+                // ---- K rows i (both 64-column halves) scaled by lambda_i into fp16; chunk order
+                // rotated by row so that 8 consecutive rows hit 8 distinct banks
+                const float lam = i < r ? tab[r - 1 - i] : 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint4 *krow = reinterpret_cast<uint4 *>(sm + OFF_KV + st * SZ_KV +
+                                                            half * 16384 + i * 128);
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; h4 += 4) {
+                        uint4 kbuf[4];
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + i) & 7];
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            krow[(h4 + ch + i) & 7] = bf16x8_to_f16x8(kbuf[ch], lam);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->k_ready);
+            } else {
+                // ---- P = A o Dm D^-0.5 into TMEM: block cb (32 key columns) goes to columns
+                // 16 cb .. 16 cb + 15 as fp16 pairs, after this warp has read A block cb (and
+                // every block it overwrites); blocks above the diagonal are zero
+                const uint32_t ta = tbase + lane_off + TM_A;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t pk[16];
+                    if (cb <= q) {
+                        uint32_t va[32];
+                        tmem_ld32(ta + (uint32_t)cb * 32u, va);
+                        tmem_ld_wait_regs(va);
+                        p_block(i, cb, va, tabp, pk);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) pk[x] = 0u;
+                    }
+                    tmem_st16(ta + (uint32_t)cb * 16u, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_ready);
+            }
+
+            // ---- state: S_c is in TMEM once MMA4 is done; hi/lo copy for MMA2_{c+1}, then
+            // e^{-s r_{c+1}} S_c back for MMA4_{c+1}
+            if (!(ok = warp_wait_bar(&bars->u_full, c & 1, limit, abort_flag, p.err))) break;
+            tc_fence_after();
+            {
+                const float dn = c + 1 < nchunks ? tab[chunk_len(kEx, cs + r, sp, n)] : 1.f;
+#pragma unroll 1
+                for (int sub = 0; sub < 2; ++sub) {
+                    const int col0 = wg * 64 + sub * 32;
+                    const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)col0;
+                    uint32_t w[32];
+                    tmem_ld32(t_s, w);
+                    tmem_ld_wait_regs(w);
+                    float S[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        S[x] = __uint_as_float(w[x]);
+                        w[x] = __float_as_uint(S[x] * dn);
+                    }
+                    tmem_st32(t_s, w);
+                    store_state_split(s_hi, s_lo, i, wg, sub, S);
+                    if (kEx && cs + r == sp)
+                        store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_ready);
+
+            // ---- out: o = gamma D^-0.5 Oint + Ointra -> bf16, 32 columns at a time
+            if (!(ok = warp_wait_bar(&bars->o_full, c & 1, limit, abort_flag, p.err))) break;
+            tc_fence_after();
+            const float gam = tabp[i + 1];
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+                const int col0 = wg * 64 + sub * 32;
+                uint32_t vi[32], vp[32];
+                tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)col0, vi);
+                tmem_ld32(tbase + lane_off + TM_OP + (uint32_t)col0, vp);
+                tmem_ld_wait_regs2(vi, vp);
+                if (sub == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->o_free);
+                }
+                uint4 ch[4];
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int x = k4 * 8 + 2 * e;
+                        w[e] = pack_bf16x2(
+                            fmaf(gam, __uint_as_float(vi[x]), __uint_as_float(vp[x])),
+                            fmaf(gam, __uint_as_float(vi[x + 1]), __uint_as_float(vp[x + 1])));
+                    }
+                    ch[k4] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                // 4x4 transpose of 16-byte chunks within each group of 4 lanes (two butterfly
+                // steps), so that store k writes row 4*(lane/4) + k of the group as one
+                // contiguous 64-byte segment per group.
+                const int pq = lane & 3;
+                {
+                    const bool lo2 = pq < 2;
+                    uint4 sa = lo2 ? ch[2] : ch[0], sb = lo2 ? ch[3] : ch[1];
+                    uint4 ra, rb;
+                    ra.x = __shfl_xor_sync(0xffffffffu, sa.x, 2);
+                    ra.y = __shfl_xor_sync(0xffffffffu, sa.y, 2);
+                    ra.z = __shfl_xor_sync(0xffffffffu, sa.z, 2);
+                    ra.w = __shfl_xor_sync(0xffffffffu, sa.w, 2);
+                    rb.x = __shfl_xor_sync(0xffffffffu, sb.x, 2);
+                    rb.y = __shfl_xor_sync(0xffffffffu, sb.y, 2);
+                    rb.z = __shfl_xor_sync(0xffffffffu, sb.z, 2);
+                    rb.w = __shfl_xor_sync(0xffffffffu, sb.w, 2);
+                    if (lo2) { ch[2] = ra; ch[3] = rb; } else { ch[0] = ra; ch[1] = rb; }
+                }
+                {
+                    const bool even = (pq & 1) == 0;
+                    uint4 sa = even ? ch[1] : ch[0], sb = even ? ch[3] : ch[2];
+                    uint4 ra, rb;
+                    ra.x = __shfl_xor_sync(0xffffffffu, sa.x, 1);
+                    ra.y = __shfl_xor_sync(0xffffffffu, sa.y, 1);
+                    ra.z = __shfl_xor_sync(0xffffffffu, sa.z, 1);
+                    ra.w = __shfl_xor_sync(0xffffffffu, sa.w, 1);
+                    rb.x = __shfl_xor_sync(0xffffffffu, sb.x, 1);
+                    rb.y = __shfl_xor_sync(0xffffffffu, sb.y, 1);
+                    rb.z = __shfl_xor_sync(0xffffffffu, sb.z, 1);
+                    rb.w = __shfl_xor_sync(0xffffffffu, sb.w, 1);
+                    if (even) { ch[1] = ra; ch[3] = rb; } else { ch[0] = ra; ch[2] = rb; }
+                }
+                // lane (4 g + pq) now holds chunk pq of rows 4 g .. 4 g + 3 of its warp's rows
+                const int rbase = q * 32 + (lane & ~3);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = rbase + k;
+                    if (row < r) {
+                        __nv_bfloat16 *dst = p.out + (size_t)(t0 + cs + row) * row_stride +
+                                             (size_t)h * head_stride + col0 + pq * 8;
+                        *reinterpret_cast<uint4 *>(dst) = ch[k];
+                    }
+                }
+            }
+        }
+        // Final state write-back (also for zero-length requests).  Skipped after an abort: the
+        // error word already reports the failure.  The last state pass left S unscaled.
+        if (ok && !*abort_flag && last_seg) {
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+                uint32_t w[32];
+                tmem_ld32(tbase + lane_off + TM_S + (uint32_t)(wg * 64 + sub * 32), w);
+                tmem_ld_wait_regs(w);
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    *reinterpret_cast<float4 *>(gstate + sub * 32 + 4 * x) = make_float4(
+                        __uint_as_float(w[4 * x]), __uint_as_float(w[4 * x + 1]),
+                        __uint_as_float(w[4 * x + 2]), __uint_as_float(w[4 * x + 3]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream) {
+    const long long units = (long long)p.B * p.H * (p.seg_len > 0 ? p.nseg : 1);
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    CUtensorMap tq, tk, tv;
+    memset(&tq, 0, sizeof(tq));
+    memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv));
+    if (p.T > 0) {
+        if (!make_token_map_full(&tq, p.q, p.T, p.H) || !make_token_map_full(&tk, p.k, p.T, p.H) ||
+            !make_token_map_full(&tv, p.v, p.T, p.H))
+            return cudaErrorInvalidValue;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[64] = {false};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev]) {
+            e = cudaFuncSetAttribute(extend_wide_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(extend_wide_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    const ExtendParams pw = p;
+    if (p.track_lens != nullptr || p.out_rs != (long long)p.H * kHeadDim || p.out_hs != kHeadDim)
+        extend_wide_kernel<true><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, pw);
+    else
+        extend_wide_kernel<false><<<(unsigned)units, kThreads, kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                    pw);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -88,9 +88,11 @@ struct SplitPlan {
     int seg_len, blk_len, nseg, nblk;
     unsigned long long ws_bytes;
 };
-SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms);
+// ctas_per_head: CTAs the extend kernel runs per (request, head, segment).
+SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_head);
 
-cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);
+cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);  // 2 CTAs per head
+cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream);     // 1 CTA per head
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
 
 }  // namespace la

@@ -12,7 +12,7 @@
 // Facts a caller needs:
 //   * The array is kNoAllocScratchBytes (16 MiB) on every device that loads this library, held
 //     until the process exits.  On a 152-SM GB300 every split plan fits (the planner never asks
-//     for more than about 12 MiB); a plan that needs more is rejected with LA_ERR_UNSUPPORTED and
+//     for more than about 14.3 MiB); a plan that needs more is rejected with LA_ERR_UNSUPPORTED and
 //     nothing is launched.
 //   * The first call on a device looks the array's device address up (cudaGetSymbolAddress, with
 //     that device current) and caches it; make that first call before any stream capture.
