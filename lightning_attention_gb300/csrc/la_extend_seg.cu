@@ -43,19 +43,21 @@ constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t SZ_T = C * kHeadDim * 2;   // one [C][128] 16-bit tile: two 16 KiB blocks
 constexpr uint32_t SZ_STAGE = 2 * SZ_T;       // K and V of one chunk
-constexpr uint32_t OFF_BAR = 2 * SZ_STAGE;
+constexpr int kStages = 3;                    // three chunks in flight hide the load latency
+constexpr uint32_t OFF_BAR = kStages * SZ_STAGE;
 constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;
 static_assert(SZ_STAGE % 1024 == 0, "atoms");
 
 struct Bars {
-    uint64_t full[2];   // TMA -> converters
-    uint64_t conv[2];   // converters -> MMA (8 warp arrivals)
-    uint64_t empty[2];  // MMA -> TMA
+    uint64_t full[kStages];   // TMA -> converters
+    uint64_t conv[kStages];   // converters -> MMA (8 warp arrivals)
+    uint64_t empty[kStages];  // MMA -> TMA
     uint64_t done;      // every MMA of the block completed
     uint32_t tmem_base;
     int abort_flag;
 };
 static_assert(sizeof(Bars) <= 128, "barrier block");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float slope = p.slopes[h];
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->conv[s], kConvWarps);
             mbar_init(&bars->empty[s], 1);
@@ -166,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1;
-                if (c >= 2 &&
-                    !wait_bar(&bars->empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                const int st = c % kStages;
+                if (c >= kStages && !wait_bar(&bars->empty[st], (c / kStages - 1) & 1, limit,
+                                              abort_flag, p.err))
                     break;
                 const int y = t0 + a + c * C;
                 const int x = h * kHeadDim;
@@ -180,29 +182,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(dst + SZ_T + 16384, &tv, &bars->full[st], x + 64, y);
                 issued = c + 1;
             }
-            for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
+            for (int c = (issued >= kStages ? issued - kStages : 0); c < issued; ++c) {
                 int dummy = 0;
-                wait_bar(&bars->full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
+                wait_bar(&bars->full[c % kStages], (c / kStages) & 1, kDrainLimitNs, &dummy,
+                         p.err);
             }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            const uint32_t idU = idesc_f16_f32(128, 64, true, true);
-            const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);        // K^T: MN-major A
-            const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 8192, 1024);  // V half: MN-major B
+            // one N = 128 MMA per 16 tokens: an M = 128 instruction costs about the same at
+            // N = 64 as at N = 128
+            const uint32_t idU = idesc_f16_f32(128, 128, true, true);
+            const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);         // K^T: MN-major A
+            const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 16384, 1024);  // V: MN-major B
             const uint64_t step = SZ_STAGE >> 4;
             for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1;
-                if (!wait_bar(&bars->conv[st], (c >> 1) & 1, limit, abort_flag, p.err)) break;
+                const int st = c % kStages;
+                if (!wait_bar(&bars->conv[st], (c / kStages) & 1, limit, abort_flag, p.err))
+                    break;
                 tc_fence_after();
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tbase + (uint32_t)half * 64u,
-                                 dK0 + st * step + (uint64_t)(kk * 128),
-                                 dV0 + st * step + (uint64_t)(half * 1024 + kk * 128), idU,
-                                 (c > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase, dK0 + st * step + (uint64_t)(kk * 128),
+                             dV0 + st * step + (uint64_t)(kk * 128), idU,
+                             (c > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars->empty[st]);
             }
             mma_commit(&bars->done);
@@ -215,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
-            const int st = c & 1;
-            if (!(ok = warp_wait_bar(&bars->full[st], (c >> 1) & 1, limit, abort_flag, p.err)))
+            const int st = c % kStages;
+            if (!(ok = warp_wait_bar(&bars->full[st], (c / kStages) & 1, limit, abort_flag,
+                                     p.err)))
                 break;
             // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
             const float lam = expf(-slope * (float)(p.blk_len - 1 - c * C - row));
