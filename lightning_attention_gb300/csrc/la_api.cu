@@ -13,8 +13,7 @@
 
 namespace {
 
-// Extend kernel: 1 = one CTA per (request, head), every MMA 128 columns wide (la_extend_w.cu);
-// 2 = two CTAs per head, one per 64-column half of the values (la_extend_tc.cu).
+// The extend kernel runs one CTA per (request, head, segment) (la_extend_w.cu).
 constexpr int kExtendCtasPerHead = 1;
 
 // Per-device error word: kernels OR bits into it when they find a fault the host cannot see
@@ -301,8 +300,7 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
-    return launch_status(kExtendCtasPerHead == 1 ? la::launch_extend_wide(p, s)
-                                                 : la::launch_extend_chunked(p, s));
+    return launch_status(la::launch_extend_wide(p, s));
 }
 
 }  // namespace

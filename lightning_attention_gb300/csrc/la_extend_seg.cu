@@ -302,7 +302,6 @@ SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_hea
     return pl;
 }
 
-bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);  // la_extend_tc.cu
 
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
     const long long ctas = (long long)p.B * p.H * p.nblk;

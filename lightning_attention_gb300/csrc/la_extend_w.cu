@@ -61,8 +61,6 @@
 
 namespace la {
 
-bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);  // la_extend_tc.cu
-
 namespace {
 
 using namespace sm100;
@@ -773,7 +771,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ----------------------------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
 }  // namespace
+
+// [T][H*128] bf16, box of 64 columns x C rows, 128-byte swizzle; rows past T read as zero.
+bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)C};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
 
 cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream) {
     const long long units = (long long)p.B * p.H * (p.seg_len > 0 ? p.nseg : 1);

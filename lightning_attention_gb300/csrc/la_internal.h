@@ -1,6 +1,7 @@
 // la_internal.h -- declarations shared by the library's translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -50,7 +51,7 @@ struct CommitParams {
 };
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream);
 
-// Chunked tensor-core extend (tcgen05 + TMA).
+// Chunked tensor-core extend (tcgen05 + TMA), one CTA per (request, head, segment).
 struct ExtendParams {
     const __nv_bfloat16 *q, *k, *v;
     const float *slopes;
@@ -91,8 +92,11 @@ struct SplitPlan {
 // ctas_per_head: CTAs the extend kernel runs per (request, head, segment).
 SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_head);
 
-cudaError_t launch_extend_chunked(const ExtendParams &p, cudaStream_t stream);  // 2 CTAs per head
-cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream);     // 1 CTA per head
+cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream);  // 1 CTA per head
+
+// [T][H*128] bf16 TMA map, box of 64 columns x 128 rows, 128-byte swizzle; rows past T read as
+// zero (la_extend_w.cu).
+bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
 
 }  // namespace la
