@@ -136,7 +136,6 @@ la_status la_decode(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     p.B = B;
     p.H = H;
     p.N = 1;
-    p.T = B;
     p.num_slots = num_slots;
     la_status st = error_word_ptr(&p.err);
     if (st != LA_OK) return st;
@@ -165,7 +164,6 @@ la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     p.B = B;
     p.H = H;
     p.N = N;
-    p.T = B * N;
     p.num_slots = num_slots;
     la_status st = error_word_ptr(&p.err);
     if (st != LA_OK) return st;
@@ -195,7 +193,6 @@ la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     p.B = B;
     p.H = H;
     p.N = N;
-    p.T = B * N;
     p.num_slots = num_slots;
     la_status st = error_word_ptr(&p.err);
     if (st != LA_OK) return st;

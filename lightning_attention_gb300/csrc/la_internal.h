@@ -20,21 +20,19 @@ enum : unsigned int {
 
 constexpr int kHeadDim = 128;
 
-// Recurrent (token-serial) kernels: decode, chain and tree verify, short extends.
-enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_EXTEND = 2, RECUR_TREE = 3 };
+// Recurrent (token-serial) kernels: decode, chain and tree verify.
+enum RecurMode : int { RECUR_DECODE = 0, RECUR_VERIFY = 1, RECUR_TREE = 3 };
 
 struct RecurParams {
     const __nv_bfloat16 *q, *k, *v;
     const float *slopes;
     float *pool;                 // [num_slots][H][D][D]
     const int32_t *state_idx;    // [B]
-    const int32_t *cu_seqlens;   // [B+1] (extend)
-    const uint8_t *prefix_mask;  // [B]   (extend)
     float *inter;                // [B][N][H][D][D] (verify)
     const int32_t *parents;      // [B][N] (tree verify)
     __nv_bfloat16 *out;
     unsigned int *err;           // device error word
-    int B, H, N, T, num_slots;
+    int B, H, N, num_slots;
 };
 
 cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream);

@@ -1,4 +1,4 @@
-// la_recurrent.cu -- token-serial seg_la kernels: one-token decode, chain verify, short extends.
+// la_recurrent.cu -- token-serial seg_la kernels: one-token decode, chain and tree verify.
 //
 // Method: page "SGLang Lightning Attention 能力矩阵与 seg_la 线性注意力测试覆盖深度解析", section
 // "独立参考实现：逐 token 递推公式":  S_t = S_{t-1} * exp(-slope_h) + outer(k_t, v_t),
@@ -56,24 +56,8 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
     }
     float *state = p.pool + ((size_t)slot * H + h) * (size_t)(kHeadDim * kHeadDim);
 
-    int t_begin, n;
-    bool from_pool = true;
-    if (MODE == RECUR_EXTEND) {
-        t_begin = p.cu_seqlens[b];
-        const int t_end = p.cu_seqlens[b + 1];
-        if (t_begin < 0 || t_end < t_begin || t_end > p.T) {
-            if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
-            return;
-        }
-        n = t_end - t_begin;
-        from_pool = p.prefix_mask[b] != 0;
-    } else if (MODE == RECUR_DECODE) {
-        t_begin = b;
-        n = 1;
-    } else {
-        t_begin = b * p.N;
-        n = p.N;
-    }
+    const int t_begin = MODE == RECUR_DECODE ? b : b * p.N;
+    const int n = MODE == RECUR_DECODE ? 1 : p.N;
     if (MODE == RECUR_TREE) {
         // parents must point backwards; checked up front so that a bad tree writes nothing
         bool bad = false;
@@ -88,15 +72,9 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
     }
 
     float4 s[kRowsPerWarp];
-    if (from_pool) {
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
-            s[r] = __ldcs(reinterpret_cast<const float4 *>(state + (size_t)(row0 + r) * kHeadDim +
-                                                           col));
-    } else {
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) s[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int r = 0; r < kRowsPerWarp; ++r)
+        s[r] = __ldcs(reinterpret_cast<const float4 *>(state + (size_t)(row0 + r) * kHeadDim + col));
 
     const float decay = expf(-p.slopes[h]);
     const size_t row_stride = (size_t)H * kHeadDim;
@@ -168,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
         // token t + 1, so one barrier per token is enough.
     }
 
-    if (MODE != RECUR_VERIFY && MODE != RECUR_TREE) {
+    if (MODE == RECUR_DECODE) {
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r)
             __stcs(reinterpret_cast<float4 *>(state + (size_t)(row0 + r) * kHeadDim + col), s[r]);
@@ -220,7 +198,6 @@ cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t 
     switch (mode) {
         case RECUR_DECODE: recurrent_kernel<RECUR_DECODE><<<grid, block, 0, stream>>>(p); break;
         case RECUR_VERIFY: recurrent_kernel<RECUR_VERIFY><<<grid, block, 0, stream>>>(p); break;
-        case RECUR_EXTEND: recurrent_kernel<RECUR_EXTEND><<<grid, block, 0, stream>>>(p); break;
         case RECUR_TREE: recurrent_kernel<RECUR_TREE><<<grid, block, 0, stream>>>(p); break;
     }
     return cudaGetLastError();
