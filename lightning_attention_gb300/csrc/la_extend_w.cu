@@ -207,16 +207,26 @@ __device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, 
 }
 
 // P row segment: 32 columns of block cb of row i, decay-masked and scaled, as 16 fp16 pairs.
-// Below the diagonal block (cb < i / 32) every i - j >= 1, so no mask is needed; in the diagonal
-// block the table is read at a clamped index and the upper triangle selected away afterwards.
+// The factor e^{-s (i - j)} D^-0.5 is, for slopes s <= kRunMaxSlope, one table read at j = 32 cb
+// followed by a running product with g = e^{s} along the row: this keeps the shared-memory loads,
+// which slow down while the MMAs stream their operands, to one per block.  The start value
+// e^{-s d} (d <= 127) may then be subnormal, but its error reaches the row only as an absolute
+// error below 2^-149 e^{31 s} < 1e-8 of the scale.  Steeper decays read the table per element.
+// In the diagonal block the columns past i are zeroed.
+constexpr float kRunMaxSlope = 2.5f;
+
 __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], const float *tabp,
-                                        uint32_t (&pk)[16]) {
-    const int d = i - cb * 32;  // i - j for jj = 0
-    if (d >= 32) {
+                                        bool run, float g, uint32_t (&pk)[16]) {
+    const int d = i - cb * 32;  // i - j for jj = 0; 0 <= d <= 127 for blocks on or below the diagonal
+    if (run) {
+        float f = tabp[d];
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 2)
-            pk[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * tabp[d - jj],
-                                     __uint_as_float(v[jj + 1]) * tabp[d - jj - 1]);
+        for (int jj = 0; jj < 32; jj += 2) {
+            const float f1 = f * g;
+            const float x0 = __uint_as_float(v[jj]) * f, x1 = __uint_as_float(v[jj + 1]) * f1;
+            pk[jj >> 1] = pack_f16x2(jj <= d ? x0 : 0.f, jj + 1 <= d ? x1 : 0.f);
+            f = f1 * g;
+        }
     } else {
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 2) {
@@ -508,6 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tab[m] = e;
             tabp[m] = e * kScale;
         }
+        const bool run = slope <= kRunMaxSlope;       // false for NaN slopes too
+        const float grow = run ? expf(slope) : 1.f;  // e^{s}: one step along a row of P
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t va[32];
                         tmem_ld32(ta + (uint32_t)cb * 32u, va);
                         tmem_ld_wait_regs(va);
-                        p_block(i, cb, va, tabp, pk);
+                        p_block(i, cb, va, tabp, run, grow, pk);
                     } else {
 #pragma unroll
                         for (int x = 0; x < 16; ++x) pk[x] = 0u;
