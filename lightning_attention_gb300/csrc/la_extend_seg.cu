@@ -16,10 +16,13 @@
 // that the extend kernel's segments never read a pool slot that the last segment rewrites.
 //
 // One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
-// two stages); eight warps scale K by e^{-s (e - 1 - t)} and convert K and V to fp16 in place; one
-// thread issues tcgen05.mma (fp16 x fp16 -> fp32) accumulating B = K_hat^T V in tensor memory over
-// the whole block; the eight warps then write B (fp32, 64 KiB) to the workspace.  The work is HBM
-// bound (64 KiB of K and V per 128 tokens, 2 x 128 x 128 x 128 MMA flops).
+// two stages); eight warps scale K by e^{-s (e - 1 - t)} into an fp16 pair hi (in place) + lo and
+// convert V to fp16 in place; one thread issues tcgen05.mma (fp16 x fp16 -> fp32) accumulating
+// B = K_hi^T V + K_lo^T V in tensor memory over the whole block; the eight warps then write B
+// (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so a
+// single fp16 K_hat would round every term by up to 2^-11, an error that the state of a slowly
+// decaying head sums over thousands of tokens; the pair keeps the terms to about 2^-22.  The work
+// is HBM bound (64 KiB of K and V per 128 tokens, 4 x 128 x 128 x 128 MMA flops).
 #include <cuda.h>
 #include <string.h>
 
@@ -42,8 +45,8 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t SZ_T = C * kHeadDim * 2;   // one [C][128] 16-bit tile: two 16 KiB blocks
-constexpr uint32_t SZ_STAGE = 2 * SZ_T;       // K and V of one chunk
-constexpr int kStages = 3;                    // three chunks in flight hide the load latency
+constexpr uint32_t SZ_STAGE = 3 * SZ_T;       // K (lambda K hi after conversion), V, lambda K lo
+constexpr int kStages = 2;
 constexpr uint32_t OFF_BAR = kStages * SZ_STAGE;
 constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;
 static_assert(SZ_STAGE % 1024 == 0, "atoms");
@@ -81,15 +84,6 @@ __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, ui
                                               volatile int *abort_flag, unsigned int *err) {
     const bool ok = wait_bar(bar, parity, limit_ns, abort_flag, err);
     return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x, float f) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
-    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -175,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int y = t0 + a + c * C;
                 const int x = h * kHeadDim;
                 uint8_t *dst = sm + st * SZ_STAGE;
-                mbar_arrive_expect_tx(&bars->full[st], SZ_STAGE);
+                mbar_arrive_expect_tx(&bars->full[st], 2 * SZ_T);
                 tma_load_2d(dst, &tk, &bars->full[st], x, y);
                 tma_load_2d(dst + 16384, &tk, &bars->full[st], x + 64, y);
                 tma_load_2d(dst + SZ_T, &tv, &bars->full[st], x, y);
@@ -195,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idU = idesc_f16_f32(128, 128, true, true);
             const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);         // K^T: MN-major A
             const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 16384, 1024);  // V: MN-major B
+            const uint64_t dKlo0 = sdesc_sw128(s_base + 2 * SZ_T, 16384, 1024);
             const uint64_t step = SZ_STAGE >> 4;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % kStages;
@@ -206,6 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tbase, dK0 + st * step + (uint64_t)(kk * 128),
                              dV0 + st * step + (uint64_t)(kk * 128), idU,
                              (c > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase, dKlo0 + st * step + (uint64_t)(kk * 128),
+                             dV0 + st * step + (uint64_t)(kk * 128), idU, 1u);
                 mma_commit(&bars->empty[st]);
             }
             mma_commit(&bars->done);
@@ -223,10 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      p.err)))
                 break;
             // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
-            const float lam = expf(-slope * (float)(p.blk_len - 1 - c * C - row));
+            const LamSplit lam = lam_split(expf(-slope * (float)(p.blk_len - 1 - c * C - row)));
             uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
             uint4 *vrow =
                 reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_T + half * 16384 + row * 128);
+            uint4 *lrow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + 2 * SZ_T + half * 16384 +
+                                                    row * 128);
             const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
             uint4 kb[8], vb[8];
 #pragma unroll
@@ -234,9 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) vb[ch] = vrow[(ch + rot) & 7];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) krow[(ch + rot) & 7] = bf16x8_to_f16x8(kb[ch], lam);
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 hi, lo;
+                bf16x8_lam_hilo(kb[ch], lam, hi, lo);
+                krow[(ch + rot) & 7] = hi;
+                lrow[(ch + rot) & 7] = lo;
+            }
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vrow[(ch + rot) & 7] = bf16x8_to_f16x8(vb[ch], 1.f);
+            for (int ch = 0; ch < 8; ++ch) vrow[(ch + rot) & 7] = bf16x8_to_f16x8(vb[ch]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->conv[st]);

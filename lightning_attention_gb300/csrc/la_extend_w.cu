@@ -85,9 +85,10 @@ constexpr float kScale = 0.08838834764831845f;
 // as two 128-byte-swizzled [128][64] blocks 16 KiB apart.
 constexpr uint32_t SZ_T = C * kHeadDim * 2;         // 32 KiB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = SZ_T;                   // stage s: K at OFF_KV + s SZ_KV, V after it
-constexpr uint32_t SZ_KV = 2 * SZ_T;
-constexpr uint32_t OFF_SHI = OFF_KV + 2 * SZ_KV;
+constexpr uint32_t OFF_K = SZ_T;                    // K of chunk c at OFF_K + (c & 1) SZ_T
+constexpr uint32_t OFF_V = OFF_K + 2 * SZ_T;        // V of the chunk in flight (one buffer)
+constexpr uint32_t OFF_KLO = OFF_V + SZ_T;          // lo half of lambda K (fp16)
+constexpr uint32_t OFF_SHI = OFF_KLO + SZ_T;
 constexpr uint32_t OFF_SLO = OFF_SHI + SZ_T;
 constexpr uint32_t OFF_TAB = OFF_SLO + SZ_T;        // e^{-s m}, m = 0..C
 constexpr uint32_t OFF_TABP = OFF_TAB + 544;        // e^{-s m} D^-0.5, m = 0..C
@@ -96,19 +97,21 @@ constexpr uint32_t SZ_BAR = 256;
 constexpr uint32_t kSmemBytes = OFF_BAR + SZ_BAR + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(OFF_BAR % 8 == 0, "barrier alignment");
-static_assert(OFF_KV % 1024 == 0 && SZ_KV % 1024 == 0 && OFF_SHI % 1024 == 0 &&
-                  OFF_SLO % 1024 == 0,
+static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_KLO % 1024 == 0 &&
+                  OFF_SHI % 1024 == 0 && OFF_SLO % 1024 == 0,
               "operand tiles start on 1024-byte swizzle atoms");
 
 struct Bars {
     uint64_t q_full;      // TMA -> all: Q of the chunk loaded
     uint64_t q_empty;     // MMA -> TMA: MMA1 and MMA2 of the chunk done with Q
-    uint64_t kv_full[2];  // TMA -> all: K, V of the chunk loaded
-    uint64_t kv_empty[2]; // MMA -> TMA: MMA3 and MMA4 of the chunk done with K and V
+    uint64_t k_full[2];   // TMA -> all: K of the chunk loaded
+    uint64_t k_empty[2];  // MMA -> TMA: MMA1 and MMA4 of the chunk done with K
+    uint64_t v_full;      // TMA -> converters: V of the chunk loaded
+    uint64_t v_empty;     // MMA -> TMA: MMA4 and MMA3 of the chunk done with V
     uint64_t a_full;      // MMA1 done
-    uint64_t v_ready[2];  // converter warps: V tile in fp16 (2 warp arrivals)
-    uint64_t k_ready;     // warps 4-7: K scaled by lambda into fp16 (4)
-    uint64_t p_ready;     // warps 0-3: P written to TMEM (4)
+    uint64_t v_ready;     // converter warps: V tile in fp16 (2 warp arrivals)
+    uint64_t k_ready;     // epilogue warps: their share of lambda K written as fp16 hi + lo (8)
+    uint64_t p_ready;     // epilogue warps: their P blocks written to TMEM (8)
     uint64_t s_ready;     // epilogue: S_hi/S_lo written, decayed S back in TMEM (8)
     uint64_t o_free;      // epilogue: Oint/Ointra read (8)
     uint64_t u_full;      // MMA4 done: S of the chunk complete (and, by issue order, MMA2)
@@ -175,16 +178,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// 16-byte chunk: 8 bf16 -> 8 fp16 times f.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x, float f) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // 32 state columns (64 atom + 32 sub .. + 31) of row `row` as bf16 hi and lo into the [128][128]
 // MN-major operand tiles.
 __device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, int row, int atom,
@@ -237,6 +230,10 @@ __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], 
         }
     }
 }
+
+// TMEM column of MMA3's A operand for k-step kk (keys 16 kk .. 16 kk + 15): P block kk / 2 sits in
+// the first 16 columns of A block kk / 2, one fp16 pair per column.
+__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); }
 
 // This thread's share of a state (row i, columns col0 .. col0 + 31) into pool slot `slot`.
 __device__ __forceinline__ void store_state_row(float *pool, int slot, int H, int h, int i,
@@ -340,13 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_empty, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
-            mbar_init(&bars->v_ready[s], kConvWarps);
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
         }
+        mbar_init(&bars->v_full, 1);
+        mbar_init(&bars->v_empty, 1);
+        mbar_init(&bars->v_ready, kConvWarps);
         mbar_init(&bars->a_full, 1);
-        mbar_init(&bars->k_ready, kEpiWarps / 2);
-        mbar_init(&bars->p_ready, kEpiWarps / 2);
+        mbar_init(&bars->k_ready, kEpiWarps);
+        mbar_init(&bars->p_ready, kEpiWarps);
         mbar_init(&bars->s_ready, kEpiWarps);
         mbar_init(&bars->o_free, kEpiWarps);
         mbar_init(&bars->u_full, 1);
@@ -375,35 +374,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int kv_issued = 0, q_issued = 0, ys = 0;
+            int k_issued = 0, q_issued = 0, v_issued = 0, ys = 0;
             const int xq = h * kHeadDim;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1;
                 const int y = t0 + (kEx ? ys : c * C);
                 if (kEx) ys += chunk_len(true, ys, sp, n);
+                // in the order the buffers free up: K (two stages), then Q after MMA2 of the
+                // previous chunk, then V after its MMA3
                 if (c >= 2 &&
-                    !wait_bar(&bars->kv_empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
+                    !wait_bar(&bars->k_empty[st], ((c >> 1) - 1) & 1, limit, abort_flag, p.err))
                     break;
-                uint8_t *kv = sm + OFF_KV + st * SZ_KV;
-                mbar_arrive_expect_tx(&bars->kv_full[st], 2 * SZ_T);
-                tma_load_2d(kv, &tk, &bars->kv_full[st], xq, y);
-                tma_load_2d(kv + 16384, &tk, &bars->kv_full[st], xq + 64, y);
-                tma_load_2d(kv + SZ_T, &tv, &bars->kv_full[st], xq, y);
-                tma_load_2d(kv + SZ_T + 16384, &tv, &bars->kv_full[st], xq + 64, y);
-                kv_issued = c + 1;
+                uint8_t *kt = sm + OFF_K + st * SZ_T;
+                mbar_arrive_expect_tx(&bars->k_full[st], SZ_T);
+                tma_load_2d(kt, &tk, &bars->k_full[st], xq, y);
+                tma_load_2d(kt + 16384, &tk, &bars->k_full[st], xq + 64, y);
+                k_issued = c + 1;
                 if (c >= 1 && !wait_bar(&bars->q_empty, (c - 1) & 1, limit, abort_flag, p.err))
                     break;
                 mbar_arrive_expect_tx(&bars->q_full, SZ_T);
                 tma_load_2d(sm + OFF_Q, &tq, &bars->q_full, xq, y);
                 tma_load_2d(sm + OFF_Q + 16384, &tq, &bars->q_full, xq + 64, y);
                 q_issued = c + 1;
+                if (c >= 1 && !wait_bar(&bars->v_empty, (c - 1) & 1, limit, abort_flag, p.err))
+                    break;
+                mbar_arrive_expect_tx(&bars->v_full, SZ_T);
+                tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq, y);
+                tma_load_2d(sm + OFF_V + 16384, &tv, &bars->v_full, xq + 64, y);
+                v_issued = c + 1;
             }
             // Copies still in flight must land before the CTA's shared memory goes away.
             int dummy = 0;
-            for (int c = (kv_issued >= 2 ? kv_issued - 2 : 0); c < kv_issued; ++c)
-                wait_bar(&bars->kv_full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
+            for (int c = (k_issued >= 2 ? k_issued - 2 : 0); c < k_issued; ++c)
+                wait_bar(&bars->k_full[c & 1], (c >> 1) & 1, kDrainLimitNs, &dummy, p.err);
             if (q_issued > 0)
                 wait_bar(&bars->q_full, (q_issued - 1) & 1, kDrainLimitNs, &dummy, p.err);
+            if (v_issued > 0)
+                wait_bar(&bars->v_full, (v_issued - 1) & 1, kDrainLimitNs, &dummy, p.err);
         }
     } else if (warp >= kConvWarp0) {
         // ------------------------------------------------------------------ V tile to fp16
@@ -412,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cl = (warp - kConvWarp0) * 32 + lane;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
-            if (!warp_wait_bar(&bars->kv_full[st], (c >> 1) & 1, limit, abort_flag, p.err))
-                break;
-            uint4 *vt = reinterpret_cast<uint4 *>(sm + OFF_KV + st * SZ_KV + SZ_T);
+            if (!warp_wait_bar(&bars->v_full, c & 1, limit, abort_flag, p.err)) break;
+            uint4 *vt = reinterpret_cast<uint4 *>(sm + OFF_V);
             constexpr int kRounds = (int)(SZ_T / 16 / (32 * kConvWarps));  // 32
 #pragma unroll
             for (int m0 = 0; m0 < kRounds; m0 += 8) {
@@ -423,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = 0; m < 8; ++m) vbuf[m] = vt[cl + 32 * kConvWarps * (m0 + m)];
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
-                    vt[cl + 32 * kConvWarps * (m0 + m)] = bf16x8_to_f16x8(vbuf[m], 1.f);
+                    vt[cl + 32 * kConvWarps * (m0 + m)] = bf16x8_to_f16x8(vbuf[m]);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->v_ready[st]);
+            if (lane == 0) mbar_arrive(&bars->v_ready);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
@@ -437,16 +443,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idP = idesc_f16_f32(128, 128, false, true);
             const uint32_t idU = idesc_f16_f32(128, 128, true, true);
             const uint64_t dQ = sdesc_sw128(s_base + OFF_Q, 16, 1024);
-            const uint64_t dK0 = sdesc_sw128(s_base + OFF_KV, 16, 1024);
-            const uint64_t dKt0 = sdesc_sw128(s_base + OFF_KV, 16384, 1024);
-            const uint64_t dV0 = sdesc_sw128(s_base + OFF_KV + SZ_T, 16384, 1024);
-            const uint64_t stage_step = SZ_KV >> 4;
+            const uint64_t dK0 = sdesc_sw128(s_base + OFF_K, 16, 1024);
+            const uint64_t dKt0 = sdesc_sw128(s_base + OFF_K, 16384, 1024);
+            const uint64_t dKlo = sdesc_sw128(s_base + OFF_KLO, 16384, 1024);
+            const uint64_t dV = sdesc_sw128(s_base + OFF_V, 16384, 1024);
+            const uint64_t stage_step = SZ_T >> 4;
             const uint64_t dHi = sdesc_sw128(s_base + OFF_SHI, 16384, 1024);
             const uint64_t dLo = sdesc_sw128(s_base + OFF_SLO, 16384, 1024);
             auto issue_qk = [&](int c) -> bool {
                 const int st = c & 1;
                 if (!wait_bar(&bars->q_full, c & 1, limit, abort_flag, p.err) ||
-                    !wait_bar(&bars->kv_full[st], (c >> 1) & 1, limit, abort_flag, p.err))
+                    !wait_bar(&bars->k_full[st], (c >> 1) & 1, limit, abort_flag, p.err))
                     return false;
                 tc_fence_after();
 #pragma unroll
@@ -476,16 +483,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bars->q_empty);
                 // S += (lambda K)^T V once K is scaled and V converted: it runs while P is built
                 if (!wait_bar(&bars->k_ready, c & 1, limit, abort_flag, p.err) ||
-                    !wait_bar(&bars->v_ready[st], (c >> 1) & 1, limit, abort_flag, p.err)) {
+                    !wait_bar(&bars->v_ready, c & 1, limit, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_S, dKt0 + st * stage_step + mnofs(kk),
-                             dV0 + st * stage_step + mnofs(kk), idU, 1);
+                    mma_bf16(tbase + TM_S, dKt0 + st * stage_step + mnofs(kk), dV + mnofs(kk), idU,
+                             1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_S, dKlo + mnofs(kk), dV + mnofs(kk), idU, 1);
                 mma_commit(&bars->u_full);
+                mma_commit(&bars->k_empty[st]);
                 // Ointra = P V once P is in TMEM: it runs while the epilogue does the state pass
                 if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err)) {
                     ok = false;
@@ -494,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_f16_tmem_a(tbase + TM_OP, tbase + TM_A + (uint32_t)(kk * 8),
-                                   dV0 + st * stage_step + mnofs(kk), idP, kk > 0);
+                    mma_f16_tmem_a(tbase + TM_OP, tbase + TM_A + p_col(kk),
+                                   dV + mnofs(kk), idP, kk > 0);
                 mma_commit(&bars->o_full);
-                mma_commit(&bars->kv_empty[st]);
+                mma_commit(&bars->v_empty);
                 if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
             }
             // Every issued MMA must finish before TMEM is freed.
@@ -511,6 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = warp >> 2;          // 64-column half for the state and output passes
         const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (S)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        // Work split of the chunk's first phase.  Lane quarter q owns P blocks 0 .. q; its two
+        // warps (q, q + 4) take the lower and upper part, and warp q + 4 zeroes the blocks above
+        // the diagonal.  The 16 lambda-K units (4 row groups x 4 column quarters) fill up the
+        // warps with fewer P blocks, a P block counting about two units:
+        //   warp   0  1  2  3  4  5  6  7
+        //   P      1  1  2  2  0  1  1  2
+        //   K      3  3  0  0  4  3  3  0
+        const int pb0 = wg ? (q + 2) >> 1 : 0;
+        const int pb1 = wg ? q + 1 : (q + 2) >> 1;
+        const bool pz = wg == 1 && q < 3;
+        // unit ranges [ku0, ku1) by warp, one byte per warp: {4,7,0,0,0,10,13,0}, {7,10,0,0,4,13,16,0}
+        const int ku0 = (int)((0x000D0A0000000704ull >> (8 * warp)) & 0xffu);
+        const int ku1 = (int)((0x00100D0400000A07ull >> (8 * warp)) & 0xffu);
 
         const float slope = p.slopes[h];
         for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
@@ -606,45 +630,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (!(ok = warp_wait_bar(&bars->a_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
-            if (wg == 1) {
-                // ---- K rows i (both 64-column halves) scaled by lambda_i into fp16; chunk order
-                // rotated by row so that 8 consecutive rows hit 8 distinct banks
-                const float lam = i < r ? tab[r - 1 - i] : 0.f;
+            // ---- lambda K as fp16 hi (in place) + lo: this warp's units of (32-row group,
+            // 32-column quarter)
+#pragma unroll 1
+            for (int u = ku0; u < ku1; ++u) {
+                const int row = (u >> 2) * 32 + lane;
+                const LamSplit lam = lam_split(row < r ? tab[r - 1 - row] : 0.f);
+                const uint32_t roff = (u & 2) * 8192 + row * 128;
+                uint4 *krow = reinterpret_cast<uint4 *>(sm + OFF_K + st * SZ_T + roff);
+                uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + roff);
+                const int h4 = (u & 1) * 4;
+                uint4 kbuf[4];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint4 *krow = reinterpret_cast<uint4 *>(sm + OFF_KV + st * SZ_KV +
-                                                            half * 16384 + i * 128);
+                for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + row) & 7];
 #pragma unroll
-                    for (int h4 = 0; h4 < 8; h4 += 4) {
-                        uint4 kbuf[4];
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + i) & 7];
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            krow[(h4 + ch + i) & 7] = bf16x8_to_f16x8(kbuf[ch], lam);
-                    }
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 hi, lo;
+                    bf16x8_lam_hilo(kbuf[ch], lam, hi, lo);
+                    krow[(h4 + ch + row) & 7] = hi;
+                    lrow[(h4 + ch + row) & 7] = lo;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->k_ready);
-            } else {
-                // ---- P = A o Dm D^-0.5 into TMEM: block cb (32 key columns) goes to columns
-                // 16 cb .. 16 cb + 15 as fp16 pairs, after this warp has read A block cb (and
-                // every block it overwrites); blocks above the diagonal are zero
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->k_ready);
+            {
+                // ---- P = A o Dm D^-0.5 into TMEM: block cb (keys 32 cb .. 32 cb + 31) goes as
+                // 16 fp16 pairs into the first 16 columns of its own A block, so a warp only
+                // overwrites what it has read itself; blocks above the diagonal are zeroed
                 const uint32_t ta = tbase + lane_off + TM_A;
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
+                for (int cb = pb0; cb < pb1; ++cb) {
                     uint32_t pk[16];
-                    if (cb <= q) {
-                        uint32_t va[32];
-                        tmem_ld32(ta + (uint32_t)cb * 32u, va);
-                        tmem_ld_wait_regs(va);
-                        p_block(i, cb, va, tabp, run, grow, pk);
-                    } else {
+                    uint32_t va[32];
+                    tmem_ld32(ta + (uint32_t)cb * 32u, va);
+                    tmem_ld_wait_regs(va);
+                    p_block(i, cb, va, tabp, run, grow, pk);
+                    tmem_st16(ta + (uint32_t)cb * 32u, pk);
+                }
+                if (pz) {
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) pk[x] = 0u;
-                    }
-                    tmem_st16(ta + (uint32_t)cb * 16u, pk);
+                    for (int x = 0; x < 16; ++x) pk[x] = 0u;
+                    for (int cb = q + 1; cb < 4; ++cb) tmem_st16(ta + (uint32_t)cb * 32u, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
