@@ -522,19 +522,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = warp >> 2;          // 64-column half for the state and output passes
         const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (S)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        // Work split of the chunk's first phase.  Lane quarter q owns P blocks 0 .. q; its two
-        // warps (q, q + 4) take the lower and upper part, and warp q + 4 zeroes the blocks above
-        // the diagonal.  The 16 lambda-K units (4 row groups x 4 column quarters) fill up the
-        // warps with fewer P blocks, a P block counting about two units:
-        //   warp   0  1  2  3  4  5  6  7
-        //   P      1  1  2  2  0  1  1  2
-        //   K      3  3  0  0  4  3  3  0
+        // Work split of the chunk's first phase.  Every warp first scales two of the 16 lambda-K
+        // units (4 row groups x 4 column quarters), so that MMA4 can start early; then lane
+        // quarter q's P blocks 0 .. q: its two warps (q, q + 4) take the lower and upper part, and
+        // warp q + 4 zeroes the blocks above the diagonal.
         const int pb0 = wg ? (q + 2) >> 1 : 0;
         const int pb1 = wg ? q + 1 : (q + 2) >> 1;
         const bool pz = wg == 1 && q < 3;
-        // unit ranges [ku0, ku1) by warp, one byte per warp: {4,7,0,0,0,10,13,0}, {7,10,0,0,4,13,16,0}
-        const int ku0 = (int)((0x000D0A0000000704ull >> (8 * warp)) & 0xffu);
-        const int ku1 = (int)((0x00100D0400000A07ull >> (8 * warp)) & 0xffu);
+        const int ku0 = 2 * warp, ku1 = 2 * warp + 2;
 
         const float slope = p.slopes[h];
         for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
