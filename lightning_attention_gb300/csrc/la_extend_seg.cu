@@ -16,7 +16,7 @@
 // that the extend kernel's segments never read a pool slot that the last segment rewrites.
 //
 // One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
-// two stages); eight warps scale K by e^{-s (e - 1 - t)} into an fp16 pair hi (in place) + lo and
+// three stages); eight warps scale K by e^{-s (e - 1 - t)} into an fp16 pair hi (in place) + lo and
 // convert V to fp16 in place; one thread issues tcgen05.mma (fp16 x fp16 -> fp32) accumulating
 // B = K_hi^T V + K_lo^T V in tensor memory over the whole block; the eight warps then write B
 // (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so a
@@ -45,9 +45,10 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t SZ_T = C * kHeadDim * 2;   // one [C][128] 16-bit tile: two 16 KiB blocks
-constexpr uint32_t SZ_STAGE = 3 * SZ_T;       // K (lambda K hi after conversion), V, lambda K lo
-constexpr int kStages = 2;
-constexpr uint32_t OFF_BAR = kStages * SZ_STAGE;
+constexpr uint32_t SZ_STAGE = 2 * SZ_T;       // K (lambda K hi after conversion) and V of a chunk
+constexpr int kStages = 3;                    // three chunks in flight hide the load latency
+constexpr uint32_t OFF_KLO = kStages * SZ_STAGE;  // lambda K lo of the chunk being multiplied
+constexpr uint32_t OFF_BAR = OFF_KLO + SZ_T;
 constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;
 static_assert(SZ_STAGE % 1024 == 0, "atoms");
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int y = t0 + a + c * C;
                 const int x = h * kHeadDim;
                 uint8_t *dst = sm + st * SZ_STAGE;
-                mbar_arrive_expect_tx(&bars->full[st], 2 * SZ_T);
+                mbar_arrive_expect_tx(&bars->full[st], SZ_STAGE);
                 tma_load_2d(dst, &tk, &bars->full[st], x, y);
                 tma_load_2d(dst + 16384, &tk, &bars->full[st], x + 64, y);
                 tma_load_2d(dst + SZ_T, &tv, &bars->full[st], x, y);
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idU = idesc_f16_f32(128, 128, true, true);
             const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);         // K^T: MN-major A
             const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 16384, 1024);  // V: MN-major B
-            const uint64_t dKlo0 = sdesc_sw128(s_base + 2 * SZ_T, 16384, 1024);
+            const uint64_t dKlo = sdesc_sw128(s_base + OFF_KLO, 16384, 1024);
             const uint64_t step = SZ_STAGE >> 4;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % kStages;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              (c > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase, dKlo0 + st * step + (uint64_t)(kk * 128),
+                    mma_bf16(tbase, dKlo + (uint64_t)(kk * 128),
                              dV0 + st * step + (uint64_t)(kk * 128), idU, 1u);
                 mma_commit(&bars->empty[st]);
             }
@@ -226,23 +227,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
             uint4 *vrow =
                 reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_T + half * 16384 + row * 128);
-            uint4 *lrow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + 2 * SZ_T + half * 16384 +
-                                                    row * 128);
+            uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + half * 16384 + row * 128);
             const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
             uint4 kb[8], vb[8];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) kb[ch] = krow[(ch + rot) & 7];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) vb[ch] = vrow[(ch + rot) & 7];
+            uint4 lo[8];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
-                uint4 hi, lo;
-                bf16x8_lam_hilo(kb[ch], lam, hi, lo);
+                uint4 hi;
+                bf16x8_lam_hilo(kb[ch], lam, hi, lo[ch]);
                 krow[(ch + rot) & 7] = hi;
-                lrow[(ch + rot) & 7] = lo;
             }
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) vrow[(ch + rot) & 7] = bf16x8_to_f16x8(vb[ch]);
+            // the lo buffer is free once the MMAs of the previous chunk are done with it
+            if (c >= 1) {
+                const int prev = (c - 1) % kStages;
+                if (!(ok = warp_wait_bar(&bars->empty[prev], ((c - 1) / kStages) & 1, limit,
+                                         abort_flag, p.err)))
+                    break;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) lrow[(ch + rot) & 7] = lo[ch];
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->conv[st]);
