@@ -16,13 +16,14 @@
 // that the extend kernel's segments never read a pool slot that the last segment rewrites.
 //
 // One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
-// three stages); eight warps scale K by e^{-s (e - 1 - t)} into an fp16 pair hi (in place) + lo and
-// convert V to fp16 in place; one thread issues tcgen05.mma (fp16 x fp16 -> fp32) accumulating
-// B = K_hi^T V + K_lo^T V in tensor memory over the whole block; the eight warps then write B
-// (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so a
-// single fp16 K_hat would round every term by up to 2^-11, an error that the state of a slowly
-// decaying head sums over thousands of tokens; the pair keeps the terms to about 2^-22.  The work
-// is HBM bound (64 KiB of K and V per 128 tokens, 4 x 128 x 128 x 128 MMA flops).
+// three stages); eight warps scale K by e^{-s (e - 1 - t)} into a bf16 pair hi (in place) + lo;
+// one thread issues tcgen05.mma (bf16 x bf16 -> fp32) accumulating B = K_hi^T V + K_lo^T V in
+// tensor memory over the whole block, V straight from the TMA tile; the eight warps then write B
+// (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so one
+// 16-bit K_hat would round every term by up to 2^-9 (bf16) or 2^-11 (fp16), an error that the
+// state of a slowly decaying head sums over thousands of tokens; the pair keeps the terms to
+// about 2^-17.  The work is HBM bound (64 KiB of K and V per 128 tokens, 4 x 128 x 128 x 128 MMA
+// flops).
 #include <cuda.h>
 #include <string.h>
 
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // one N = 128 MMA per 16 tokens: an M = 128 instruction costs about the same at
             // N = 64 as at N = 128
-            const uint32_t idU = idesc_f16_f32(128, 128, true, true);
+            const uint32_t idU = idesc_bf16_f32(128, 128, true, true);
             const uint64_t dK0 = sdesc_sw128(s_base, 16384, 1024);         // K^T: MN-major A
             const uint64_t dV0 = sdesc_sw128(s_base + SZ_T, 16384, 1024);  // V: MN-major B
             const uint64_t dKlo = sdesc_sw128(s_base + OFF_KLO, 16384, 1024);
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // converters / epilogue: thread pair (2 row, 2 row + 1) owns row `row` of the chunk; each
-        // converts one 64-column half of K and of V
+        // scales one 64-column half of K
         const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
@@ -223,26 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      p.err)))
                 break;
             // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
-            const LamSplit lam = lam_split(expf(-slope * (float)(p.blk_len - 1 - c * C - row)));
+            const float lam = expf(-slope * (float)(p.blk_len - 1 - c * C - row));
             uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
-            uint4 *vrow =
-                reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + SZ_T + half * 16384 + row * 128);
             uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + half * 16384 + row * 128);
             const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
-            uint4 kb[8], vb[8];
+            uint4 kb[8];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) kb[ch] = krow[(ch + rot) & 7];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vb[ch] = vrow[(ch + rot) & 7];
             uint4 lo[8];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
                 uint4 hi;
-                bf16x8_lam_hilo(kb[ch], lam, hi, lo[ch]);
+                bf16x8_scale_hilo_bf16(kb[ch], lam, hi, lo[ch]);
                 krow[(ch + rot) & 7] = hi;
             }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vrow[(ch + rot) & 7] = bf16x8_to_f16x8(vb[ch]);
             // the lo buffer is free once the MMAs of the previous chunk are done with it
             if (c >= 1) {
                 const int prev = (c - 1) % kStages;

@@ -315,6 +315,43 @@ __device__ __forceinline__ void bf16x8_lam_hilo(const uint4 x, const LamSplit &l
     lo = make_uint4(lv[0], lv[1], lv[2], lv[3]);
 }
 
+// The two halves separately (the same arithmetic, so hi + lo is the pair above).
+__device__ __forceinline__ uint4 bf16x8_lam_hi(const uint4 x, const LamSplit &l) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __half2 k = __floats2half2_rn(__uint_as_float(w[e] << 16),
+                                            __uint_as_float(w[e] & 0xffff0000u));
+        const __half2 a = __hmul2(l.l1, k);
+        hv[e] = *reinterpret_cast<const uint32_t *>(&a);
+    }
+    return make_uint4(hv[0], hv[1], hv[2], hv[3]);
+}
+__device__ __forceinline__ uint4 bf16x8_lam_lo(const uint4 x, const LamSplit &l) {
+    uint4 hi, lo;
+    bf16x8_lam_hilo(x, l, hi, lo);
+    return lo;
+}
+
+// 16-byte chunk: 8 bf16 K values times f as a bf16 pair hi + lo, hi = bf16(K f) and
+// lo = bf16(K f - hi), the product and the difference exact in fp32: the pair carries K f to about
+// 2^-17 relative (hi alone: 2^-8).
+__device__ __forceinline__ void bf16x8_scale_hilo_bf16(const uint4 x, float f, uint4 &hi,
+                                                       uint4 &lo) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t hv[4], lv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = __uint_as_float(w[e] << 16) * f, b = __uint_as_float(w[e] & 0xffff0000u) * f;
+        const uint32_t hb = pack_bf16x2(a, b);
+        hv[e] = hb;
+        lv[e] = pack_bf16x2(a - __uint_as_float(hb << 16), b - __uint_as_float(hb & 0xffff0000u));
+    }
+    hi = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    lo = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+}
+
 // 16-byte chunk: 8 bf16 -> 8 fp16 (exact for values in fp16's normal range).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
