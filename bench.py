@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -165,8 +166,22 @@ def read_peaks():
 
 
 def source_digest(fname: str) -> str:
-    with open(os.path.join(ROOT, "lightning_attention_gb300", "csrc", fname), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Digest of a kernel's source file and the local headers it includes (recursively)."""
+    csrc = os.path.join(ROOT, "lightning_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    seen, todo = set(), [fname]
+    while todo:
+        name = todo.pop(0)
+        if name in seen:
+            continue
+        seen.add(name)
+        with open(os.path.join(csrc, name), "rb") as f:
+            text = f.read()
+        h.update(text)
+        for inc in re.findall(rb'^#include "([^"]+)"', text, flags=re.M):
+            if os.path.exists(os.path.join(csrc, inc.decode())):
+                todo.append(inc.decode())
+    return h.hexdigest()[:16]
 
 
 def stored_traffic(workload: str):
