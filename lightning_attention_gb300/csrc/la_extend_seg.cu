@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      p.err)))
                 break;
             // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
-            const float lam = expf(-slope * (float)(p.blk_len - 1 - c * C - row));
+            const LamSplitBf lam =
+                lam_split_bf16(expf(-slope * (float)(p.blk_len - 1 - c * C - row)));
             uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
             uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + half * 16384 + row * 128);
             const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
                 uint4 hi;
-                bf16x8_scale_hilo_bf16(kb[ch], lam, hi, lo[ch]);
+                bf16x8_lam_hilo_bf16(kb[ch], lam, hi, lo[ch]);
                 krow[(ch + rot) & 7] = hi;
             }
             // the lo buffer is free once the MMAs of the previous chunk are done with it

@@ -18,34 +18,41 @@
 // Why one CTA per head.  An M = 128 tcgen05.mma costs about the same whether N is 64 or 128, so
 // covering all 128 value columns in one CTA halves the MMA instructions per head and chunk, and
 // the score matrix Q K^T and its mask are built once per head instead of once per column half.
-// What it costs is storage: the value tile doubles, so Q has a single shared-memory buffer (K and
-// V keep two), P moves into tensor memory in place of Q K^T, and the state update accumulates
-// straight into the fp32 master state in tensor memory (pre-scaled by the next chunk's decay)
-// instead of into a separate U buffer.
+// What it costs is storage: the value tile doubles, so Q and V have a single shared-memory buffer
+// each (K keeps two), P moves into tensor memory in place of Q K^T, and the state update
+// accumulates straight into the fp32 master state in tensor memory (pre-scaled by the next
+// chunk's decay) instead of into a separate U buffer.
 //
-// Roles (384 threads):
-//   warp 8      TMA producer: K and V of each chunk into a two-stage ring, Q into its buffer once
-//               the previous chunk's Q products are done;
-//   warps 10-11 convert each landed V tile (128 x 128) to fp16 in place;
-//   warp 9      TMEM allocator and MMA issuer (one thread), all accumulating in fp32:
-//                 MMA1  A       = Q K^T              bf16 x bf16  -> TMEM (128 columns)
-//                 MMA2  Oint    = Q S_hi + Q S_lo    bf16 x bf16  -> TMEM (128 columns)
-//                 MMA4  S      += (lambda K)^T V     fp16 x fp16  -> TMEM (the state itself)
-//                 MMA3  Ointra  = P V                fp16 (P from TMEM) x fp16
-//   warps 0-3   P: read A for their 32 rows, write P = A o Dm D^-0.5 as fp16 pairs over the first
-//               64 TMEM columns of A (every read of a row happens in the warp that overwrites it);
-//   warps 4-7   scale K by lambda into fp16 in place (both 64-column halves of their 32 rows);
-//   warps 0-7   then, per 64-column half (warp / 4): the state pass (S to bf16 hi + lo in shared
-//               memory for MMA2, snapshot if tracked, S times the next chunk's decay back to TMEM)
-//               and the output pass (gamma D^-0.5 Oint + Ointra -> bf16 -> global).
+// Precision.  Every product runs in bf16 with fp32 accumulation, and the three operands that are
+// computed in the kernel carry a bf16 pair hi + lo (about 2^-17): the state for Q S, P for P V,
+// and lambda K for the state update.  A single 16-bit lambda K rounds each term of the state
+// update, which a slowly decaying head sums over thousands of tokens; a single bf16 P or state
+// operand breaks the parity bound outright.  V and K are used as loaded.
+//
+// Roles (320 threads):
+//   warp 8      TMA producer: K of each chunk into a two-stage ring; Q and V into their buffers
+//               once the previous chunk's products with them are done;
+//   warp 9      TMEM allocator and MMA issuer (one thread), all bf16 with fp32 accumulation:
+//                 MMA1  A       = Q K^T                            -> TMEM (128 columns)
+//                 MMA2  Oint    = Q S_hi + Q S_lo                  -> TMEM (128 columns)
+//                 MMA4  S      += (lambda K)_hi^T V + (lambda K)_lo^T V   -> TMEM (the state)
+//                 MMA3  Ointra  = P_hi V + P_lo V  (P from TMEM)   -> TMEM (128 columns)
+//   warps 0-7   first phase: two units of lambda K each (32 rows x 32 columns; hi in place, lo
+//               into its own buffer), then the P blocks of their TMEM lane quarter (warp % 4):
+//               P = A o Dm D^-0.5 for 32 keys as hi + lo over that block's 32 columns of A (every
+//               read of a row happens in the warp that overwrites it); then, per 64-column half
+//               (warp / 4): the state pass (S to bf16 hi + lo in shared memory for MMA2, snapshot
+//               if tracked, S times the next chunk's decay back to TMEM) and the output pass
+//               (gamma D^-0.5 Oint + Ointra -> bf16 -> global).
 // TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128.
 //
 // Per chunk c, the MMA thread issues MMA2_c (after the state pass of c-1 and the output pass of
-// c-1), MMA4_c (after K is scaled and V converted), MMA3_c (after P), then MMA1_{c+1}.  The
+// c-1), MMA4_c (after K is scaled and V has landed), MMA3_c (after P), then MMA1_{c+1}.  The
 // orders that make the buffer reuse safe: MMA1_{c+1} overwrites A/P after MMA3_c by issue order;
 // P_c is written after MMA1_c is complete; the state pass of c rewrites S_hi/S_lo after u_full(c),
 // which also covers MMA2_c; MMA4_c accumulates into S after the state pass of c-1 has scaled it;
-// Q_{c+1} is loaded after MMA2_c (and so MMA1_c) is complete.
+// the lambda-K lo buffer is rewritten after MMA1_c, hence after MMA4_{c-1}; Q_{c+1} is loaded after
+// MMA2_c (and so MMA1_c) is complete, V_{c+1} after MMA3_c.
 //
 // Every mbarrier wait is bounded (a globaltimer deadline).  A wait that runs out sets the error
 // word and an abort flag; every role then leaves its loop, the producer waits for its own copies
@@ -70,11 +77,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kConvWarp0 = 10;      // warps 10, 11: V tile to fp16
-constexpr int kConvWarps = 2;
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_A = 0;        // 128 columns: Q K^T (fp32); P (fp16 pairs) in columns 0-63
+constexpr uint32_t TM_A = 0;        // 128 columns: Q K^T (fp32), then P (bf16 hi + lo pairs)
 constexpr uint32_t TM_OI = 128;     // 128 columns: Q S
 constexpr uint32_t TM_OP = 256;     // 128 columns: P V
 constexpr uint32_t TM_S = 384;      // 128 columns: the fp32 master state
@@ -87,7 +92,7 @@ constexpr uint32_t SZ_T = C * kHeadDim * 2;         // 32 KiB
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = SZ_T;                    // K of chunk c at OFF_K + (c & 1) SZ_T
 constexpr uint32_t OFF_V = OFF_K + 2 * SZ_T;        // V of the chunk in flight (one buffer)
-constexpr uint32_t OFF_KLO = OFF_V + SZ_T;          // lo half of lambda K (fp16)
+constexpr uint32_t OFF_KLO = OFF_V + SZ_T;          // lo half of lambda K (bf16)
 constexpr uint32_t OFF_SHI = OFF_KLO + SZ_T;
 constexpr uint32_t OFF_SLO = OFF_SHI + SZ_T;
 constexpr uint32_t OFF_TAB = OFF_SLO + SZ_T;        // e^{-s m}, m = 0..C
@@ -109,8 +114,7 @@ struct Bars {
     uint64_t v_full;      // TMA -> converters: V of the chunk loaded
     uint64_t v_empty;     // MMA -> TMA: MMA4 and MMA3 of the chunk done with V
     uint64_t a_full;      // MMA1 done
-    uint64_t v_ready;     // converter warps: V tile in fp16 (2 warp arrivals)
-    uint64_t k_ready;     // epilogue warps: their share of lambda K written as fp16 hi + lo (8)
+    uint64_t k_ready;     // epilogue warps: their share of lambda K written as hi + lo (8)
     uint64_t p_ready;     // epilogue warps: their P blocks written to TMEM (8)
     uint64_t s_ready;     // epilogue: S_hi/S_lo written, decayed S back in TMEM (8)
     uint64_t o_free;      // epilogue: Oint/Ointra read (8)
@@ -155,8 +159,9 @@ __device__ __forceinline__ uint64_t kofs(int kk) {
 }
 __device__ __forceinline__ uint64_t mnofs(int kk) { return (uint64_t)(kk * 128); }
 
-// D[tmem] (+)= A[tmem] * B[smem], fp16 operands, fp32 accumulate; issued by one thread.  A is
-// M = 128 lanes by K = 16 values, two fp16 values per 32-bit column (even index in the low half).
+// D[tmem] (+)= A[tmem] * B[smem], 16-bit operands (the type is in idesc), fp32 accumulate; issued
+// by one thread.  A is M = 128 lanes by K = 16 values, two values per 32-bit column (even index in
+// the low half).
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -199,7 +204,8 @@ __device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, 
     }
 }
 
-// P row segment: 32 columns of block cb of row i, decay-masked and scaled, as 16 fp16 pairs.
+// P row segment: 32 columns of block cb of row i, decay-masked and scaled, as a bf16 pair hi + lo
+// (16 words each; hi = bf16(x), lo = bf16(x - hi), about 2^-17 together).
 // The factor e^{-s (i - j)} D^-0.5 is, for slopes s <= kRunMaxSlope, one table read at j = 32 cb
 // followed by a running product with g = e^{s} along the row: this keeps the shared-memory loads,
 // which slow down while the MMAs stream their operands, to one per block.  The start value
@@ -208,8 +214,13 @@ __device__ __forceinline__ void store_state_split(uint8_t *s_hi, uint8_t *s_lo, 
 // In the diagonal block the columns past i are zeroed.
 constexpr float kRunMaxSlope = 2.5f;
 
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(x0, x1);
+    lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
 __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], const float *tabp,
-                                        bool run, float g, uint32_t (&pk)[16]) {
+                                        bool run, float g, uint32_t (&ph)[16], uint32_t (&pl)[16]) {
     const int d = i - cb * 32;  // i - j for jj = 0; 0 <= d <= 127 for blocks on or below the diagonal
     if (run) {
         float f = tabp[d];
@@ -217,7 +228,7 @@ __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], 
         for (int jj = 0; jj < 32; jj += 2) {
             const float f1 = f * g;
             const float x0 = __uint_as_float(v[jj]) * f, x1 = __uint_as_float(v[jj + 1]) * f1;
-            pk[jj >> 1] = pack_f16x2(jj <= d ? x0 : 0.f, jj + 1 <= d ? x1 : 0.f);
+            split_bf16x2(jj <= d ? x0 : 0.f, jj + 1 <= d ? x1 : 0.f, ph[jj >> 1], pl[jj >> 1]);
             f = f1 * g;
         }
     } else {
@@ -226,13 +237,14 @@ __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], 
             const int d0 = d - jj, d1 = d - jj - 1;
             const float x0 = __uint_as_float(v[jj]) * tabp[max(d0, 0)];
             const float x1 = __uint_as_float(v[jj + 1]) * tabp[max(d1, 0)];
-            pk[jj >> 1] = pack_f16x2(d0 >= 0 ? x0 : 0.f, d1 >= 0 ? x1 : 0.f);
+            split_bf16x2(d0 >= 0 ? x0 : 0.f, d1 >= 0 ? x1 : 0.f, ph[jj >> 1], pl[jj >> 1]);
         }
     }
 }
 
 // TMEM column of MMA3's A operand for k-step kk (keys 16 kk .. 16 kk + 15): P block kk / 2 sits in
-// the first 16 columns of A block kk / 2, one fp16 pair per column.
+// A block kk / 2, its hi half in the first 16 columns and its lo half in the next 16, one bf16
+// pair per column.
 __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); }
 
 // This thread's share of a state (row i, columns col0 .. col0 + 31) into pool slot `slot`.
@@ -342,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->v_full, 1);
         mbar_init(&bars->v_empty, 1);
-        mbar_init(&bars->v_ready, kConvWarps);
         mbar_init(&bars->a_full, 1);
         mbar_init(&bars->k_ready, kEpiWarps);
         mbar_init(&bars->p_ready, kEpiWarps);
@@ -412,36 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (v_issued > 0)
                 wait_bar(&bars->v_full, (v_issued - 1) & 1, kDrainLimitNs, &dummy, p.err);
         }
-    } else if (warp >= kConvWarp0) {
-        // ------------------------------------------------------------------ V tile to fp16
-        // Two warps convert each landed V tile in place (32 KiB, 16-byte chunks, 64 consecutive
-        // chunks per round), well before MMA4 and MMA3 need it.
-        const int cl = (warp - kConvWarp0) * 32 + lane;
-        for (int c = 0; c < nchunks; ++c) {
-            const int st = c & 1;
-            if (!warp_wait_bar(&bars->v_full, c & 1, limit, abort_flag, p.err)) break;
-            uint4 *vt = reinterpret_cast<uint4 *>(sm + OFF_V);
-            constexpr int kRounds = (int)(SZ_T / 16 / (32 * kConvWarps));  // 32
-#pragma unroll
-            for (int m0 = 0; m0 < kRounds; m0 += 8) {
-                uint4 vbuf[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) vbuf[m] = vt[cl + 32 * kConvWarps * (m0 + m)];
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    vt[cl + 32 * kConvWarps * (m0 + m)] = bf16x8_to_f16x8(vbuf[m]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->v_ready);
-        }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idA = idesc_bf16_f32(128, 128, false, false);
             const uint32_t idI = idesc_bf16_f32(128, 128, false, true);
-            const uint32_t idP = idesc_f16_f32(128, 128, false, true);
-            const uint32_t idU = idesc_f16_f32(128, 128, true, true);
+            const uint32_t idP = idesc_bf16_f32(128, 128, false, true);
+            const uint32_t idU = idesc_bf16_f32(128, 128, true, true);
             const uint64_t dQ = sdesc_sw128(s_base + OFF_Q, 16, 1024);
             const uint64_t dK0 = sdesc_sw128(s_base + OFF_K, 16, 1024);
             const uint64_t dKt0 = sdesc_sw128(s_base + OFF_K, 16384, 1024);
@@ -483,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bars->q_empty);
                 // S += (lambda K)^T V once K is scaled and V converted: it runs while P is built
                 if (!wait_bar(&bars->k_ready, c & 1, limit, abort_flag, p.err) ||
-                    !wait_bar(&bars->v_ready, c & 1, limit, abort_flag, p.err)) {
+                    !wait_bar(&bars->v_full, c & 1, limit, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
@@ -507,6 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; ++kk)
                     mma_f16_tmem_a(tbase + TM_OP, tbase + TM_A + p_col(kk),
                                    dV + mnofs(kk), idP, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_tmem_a(tbase + TM_OP, tbase + TM_A + p_col(kk) + 16u,
+                                   dV + mnofs(kk), idP, 1);
                 mma_commit(&bars->o_full);
                 mma_commit(&bars->v_empty);
                 if (c + 1 < nchunks && !(ok = issue_qk(c + 1))) break;
@@ -625,12 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (!(ok = warp_wait_bar(&bars->a_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
-            // ---- lambda K as fp16 hi (in place) + lo: this warp's units of (32-row group,
+            // ---- lambda K as a bf16 pair hi (in place) + lo: this warp's units of (32-row group,
             // 32-column quarter)
 #pragma unroll 1
             for (int u = ku0; u < ku1; ++u) {
                 const int row = (u >> 2) * 32 + lane;
-                const LamSplit lam = lam_split(row < r ? tab[r - 1 - row] : 0.f);
+                const LamSplitBf lam = lam_split_bf16(row < r ? tab[r - 1 - row] : 0.f);
                 const uint32_t roff = (u & 2) * 8192 + row * 128;
                 uint4 *krow = reinterpret_cast<uint4 *>(sm + OFF_K + st * SZ_T + roff);
                 uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + roff);
@@ -641,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint4 hi, lo;
-                    bf16x8_lam_hilo(kbuf[ch], lam, hi, lo);
+                    bf16x8_lam_hilo_bf16(kbuf[ch], lam, hi, lo);
                     krow[(h4 + ch + row) & 7] = hi;
                     lrow[(h4 + ch + row) & 7] = lo;
                 }
@@ -650,24 +642,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->k_ready);
             {
-                // ---- P = A o Dm D^-0.5 into TMEM: block cb (keys 32 cb .. 32 cb + 31) goes as
-                // 16 fp16 pairs into the first 16 columns of its own A block, so a warp only
-                // overwrites what it has read itself; blocks above the diagonal are zeroed
+                // ---- P = A o Dm D^-0.5 into TMEM: block cb (keys 32 cb .. 32 cb + 31) goes as a
+                // bf16 pair hi + lo over its own A block's 32 columns, so a warp only overwrites
+                // what it has read itself; blocks above the diagonal are zeroed
                 const uint32_t ta = tbase + lane_off + TM_A;
 #pragma unroll 1
                 for (int cb = pb0; cb < pb1; ++cb) {
-                    uint32_t pk[16];
+                    uint32_t ph[16], pl[16];
                     uint32_t va[32];
                     tmem_ld32(ta + (uint32_t)cb * 32u, va);
                     tmem_ld_wait_regs(va);
-                    p_block(i, cb, va, tabp, run, grow, pk);
-                    tmem_st16(ta + (uint32_t)cb * 32u, pk);
+                    p_block(i, cb, va, tabp, run, grow, ph, pl);
+                    tmem_st16(ta + (uint32_t)cb * 32u, ph);
+                    tmem_st16(ta + (uint32_t)cb * 32u + 16u, pl);
                 }
                 if (pz) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) pk[x] = 0u;
-                    for (int cb = q + 1; cb < 4; ++cb) tmem_st16(ta + (uint32_t)cb * 32u, pk);
+                    for (int cb = q + 1; cb < 4; ++cb) {
+                        tmem_st16(ta + (uint32_t)cb * 32u, pk);
+                        tmem_st16(ta + (uint32_t)cb * 32u + 16u, pk);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();

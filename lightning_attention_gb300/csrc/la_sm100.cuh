@@ -282,84 +282,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-
-// lambda K as an fp16 pair hi + lo, by the error-free product transform in fp16 arithmetic:
-// lambda = l1 + l2 with l1 = fp16(lambda) and l2 = fp16(lambda - l1); a bf16 K is exact in fp16;
-// hi = fp16(l1 K), the fused e = l1 K - hi is exact, and lo = fp16(l2 K + e).  The pair carries
-// lambda K to about 2^-22 relative (absolute 2^-24 where the terms fall below fp16's normal
-// range), where hi alone rounds it to 2^-11: an error that a state with a long memory (slow
-// decay) sums coherently over thousands of tokens.
-struct LamSplit {
-    __half2 l1, l2;
+// lambda K as a bf16 pair hi + lo, by the error-free product transform in bf16 arithmetic:
+// lambda = l1 + l2 with l1 = bf16(lambda) and l2 = bf16(lambda - l1); hi = bf16(l1 K), the fused
+// e = l1 K - hi is exact (the 16-bit product minus its 8-bit rounding fits 8 bits), and
+// lo = bf16(l2 K + e).  The pair carries lambda K to about 2^-17 relative in three bf16x2
+// instructions per two values.
+struct LamSplitBf {
+    __nv_bfloat162 l1, l2;
 };
-__device__ __forceinline__ LamSplit lam_split(float lam) {
-    const __half h = __float2half_rn(lam);
-    return {__half2half2(h), __float2half2_rn(lam - __half2float(h))};
+__device__ __forceinline__ LamSplitBf lam_split_bf16(float lam) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(lam);
+    return {__bfloat162bfloat162(h), __bfloat162bfloat162(__float2bfloat16_rn(lam - __bfloat162float(h)))};
 }
-// 16-byte chunk: 8 bf16 K values -> hi and lo of lambda K as 8 fp16 each.
-__device__ __forceinline__ void bf16x8_lam_hilo(const uint4 x, const LamSplit &l, uint4 &hi,
-                                                uint4 &lo) {
+__device__ __forceinline__ void bf16x8_lam_hilo_bf16(const uint4 x, const LamSplitBf &l, uint4 &hi,
+                                                     uint4 &lo) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t hv[4], lv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const __half2 k = __floats2half2_rn(__uint_as_float(w[e] << 16),
-                                            __uint_as_float(w[e] & 0xffff0000u));
-        const __half2 a = __hmul2(l.l1, k);
-        const __half2 err = __hfma2(l.l1, k, __hneg2(a));
-        const __half2 b = __hfma2(l.l2, k, err);
+        const __nv_bfloat162 k = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+        const __nv_bfloat162 a = __hmul2(l.l1, k);
+        const __nv_bfloat162 err = __hfma2(l.l1, k, __hneg2(a));
+        const __nv_bfloat162 b = __hfma2(l.l2, k, err);
         hv[e] = *reinterpret_cast<const uint32_t *>(&a);
         lv[e] = *reinterpret_cast<const uint32_t *>(&b);
     }
     hi = make_uint4(hv[0], hv[1], hv[2], hv[3]);
     lo = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-}
-
-// The two halves separately (the same arithmetic, so hi + lo is the pair above).
-__device__ __forceinline__ uint4 bf16x8_lam_hi(const uint4 x, const LamSplit &l) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t hv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __half2 k = __floats2half2_rn(__uint_as_float(w[e] << 16),
-                                            __uint_as_float(w[e] & 0xffff0000u));
-        const __half2 a = __hmul2(l.l1, k);
-        hv[e] = *reinterpret_cast<const uint32_t *>(&a);
-    }
-    return make_uint4(hv[0], hv[1], hv[2], hv[3]);
-}
-__device__ __forceinline__ uint4 bf16x8_lam_lo(const uint4 x, const LamSplit &l) {
-    uint4 hi, lo;
-    bf16x8_lam_hilo(x, l, hi, lo);
-    return lo;
-}
-
-// 16-byte chunk: 8 bf16 K values times f as a bf16 pair hi + lo, hi = bf16(K f) and
-// lo = bf16(K f - hi), the product and the difference exact in fp32: the pair carries K f to about
-// 2^-17 relative (hi alone: 2^-8).
-__device__ __forceinline__ void bf16x8_scale_hilo_bf16(const uint4 x, float f, uint4 &hi,
-                                                       uint4 &lo) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t hv[4], lv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float a = __uint_as_float(w[e] << 16) * f, b = __uint_as_float(w[e] & 0xffff0000u) * f;
-        const uint32_t hb = pack_bf16x2(a, b);
-        hv[e] = hb;
-        lv[e] = pack_bf16x2(a - __uint_as_float(hb << 16), b - __uint_as_float(hb & 0xffff0000u));
-    }
-    hi = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-    lo = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-}
-
-// 16-byte chunk: 8 bf16 -> 8 fp16 (exact for values in fp16's normal range).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 x) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        o[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
-    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace sm100
