@@ -713,11 +713,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)col0, vi);
                 tmem_ld32(tbase + lane_off + TM_OP + (uint32_t)col0, vp);
                 tmem_ld_wait_regs2(vi, vp);
-                if (sub == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->o_free);
-                }
                 uint4 ch[4];
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
@@ -775,6 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_free);
         }
         // Final state write-back (also for zero-length requests).  Skipped after an abort: the
         // error word already reports the failure.  The last state pass left S unscaled.
