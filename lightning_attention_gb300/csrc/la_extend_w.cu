@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb0 = wg ? (q + 2) >> 1 : 0;
         const int pb1 = wg ? q + 1 : (q + 2) >> 1;
         const bool pz = wg == 1 && q < 3;
-        const int ku0 = 2 * warp, ku1 = 2 * warp + 2;
+        const int ku0 = 2 * warp;  // units ku0 and ku0 + 1
 
         const float slope = p.slopes[h];
         for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
@@ -619,23 +619,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // ---- lambda K as a bf16 pair hi (in place) + lo: this warp's units of (32-row group,
             // 32-column quarter)
-#pragma unroll 1
-            for (int u = ku0; u < ku1; ++u) {
-                const int row = (u >> 2) * 32 + lane;
-                const LamSplitBf lam = lam_split_bf16(row < r ? tab[r - 1 - row] : 0.f);
-                const uint32_t roff = (u & 2) * 8192 + row * 128;
-                uint4 *krow = reinterpret_cast<uint4 *>(sm + OFF_K + st * SZ_T + roff);
-                uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + roff);
-                const int h4 = (u & 1) * 4;
-                uint4 kbuf[4];
+            // both units' loads are issued before either is converted, so the warp waits for
+            // one shared-memory round trip instead of two
+            {
+                uint4 kbuf[2][4];
+                uint4 *krow[2];
+                uint4 *lrow[2];
+                int rr[2], h4[2];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) kbuf[ch] = krow[(h4 + ch + row) & 7];
+                for (int k = 0; k < 2; ++k) {
+                    const int u = ku0 + k;
+                    rr[k] = (u >> 2) * 32 + lane;
+                    const uint32_t roff = (u & 2) * 8192 + rr[k] * 128;
+                    krow[k] = reinterpret_cast<uint4 *>(sm + OFF_K + st * SZ_T + roff);
+                    lrow[k] = reinterpret_cast<uint4 *>(sm + OFF_KLO + roff);
+                    h4[k] = (u & 1) * 4;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint4 hi, lo;
-                    bf16x8_lam_hilo_bf16(kbuf[ch], lam, hi, lo);
-                    krow[(h4 + ch + row) & 7] = hi;
-                    lrow[(h4 + ch + row) & 7] = lo;
+                    for (int ch = 0; ch < 4; ++ch) kbuf[k][ch] = krow[k][(h4[k] + ch + rr[k]) & 7];
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const LamSplitBf lam = lam_split_bf16(rr[k] < r ? tab[r - 1 - rr[k]] : 0.f);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 hi, lo;
+                        bf16x8_lam_hilo_bf16(kbuf[k][ch], lam, hi, lo);
+                        krow[k][(h4[k] + ch + rr[k]) & 7] = hi;
+                        lrow[k][(h4[k] + ch + rr[k]) & 7] = lo;
+                    }
                 }
             }
             fence_proxy_async_smem();
