@@ -220,10 +220,11 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
 }
 
 __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], const float *tabp,
-                                        bool run, float g, uint32_t (&ph)[16], uint32_t (&pl)[16]) {
+                                        bool run, float g, float f0, uint32_t (&ph)[16],
+                                        uint32_t (&pl)[16]) {
     const int d = i - cb * 32;  // i - j for jj = 0; 0 <= d <= 127 for blocks on or below the diagonal
     if (run) {
-        float f = tabp[d];
+        float f = f0;  // tabp[d], read by the caller once per kernel
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 2) {
             const float f1 = f * g;
@@ -608,6 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t head_stride = kEx ? (size_t)p.out_hs : (size_t)kHeadDim;
         bool ok = true;
         int cs_next = 0;
+        // Table values that stay fixed for every full chunk, read once: table reads inside the
+        // chunk are slow while the MMAs stream their operands.
+        const float gam = tabp[i + 1];     // gamma_i D^-0.5
+        const float dn_full = tab[C];      // decay over a full chunk
+        LamSplitBf lam_full[2];            // lambda of this warp's two K units' rows, full chunk
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            lam_full[k] = lam_split_bf16(tab[C - 1 - (((ku0 + k) >> 2) * 32 + lane)]);
+        // P start factors e^{-s (i - 32 cb)} D^-0.5 of this warp's (at most two) blocks
+        const float f_p0 = pb0 < pb1 ? tabp[i - 32 * pb0] : 0.f;
+        const float f_p1 = pb0 + 1 < pb1 ? tabp[i - 32 * (pb0 + 1)] : 0.f;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
             // first token of the chunk and its length
@@ -639,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const LamSplitBf lam = lam_split_bf16(rr[k] < r ? tab[r - 1 - rr[k]] : 0.f);
+                    const LamSplitBf lam = r == C ? lam_full[k]
+                                                  : lam_split_bf16(rr[k] < r ? tab[r - 1 - rr[k]] : 0.f);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         uint4 hi, lo;
@@ -663,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t va[32];
                     tmem_ld32(ta + (uint32_t)cb * 32u, va);
                     tmem_ld_wait_regs(va);
-                    p_block(i, cb, va, tabp, run, grow, ph, pl);
+                    p_block(i, cb, va, tabp, run, grow, cb == pb0 ? f_p0 : f_p1, ph, pl);
                     tmem_st16(ta + (uint32_t)cb * 32u, ph);
                     tmem_st16(ta + (uint32_t)cb * 32u + 16u, pl);
                 }
@@ -687,7 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->u_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
             {
-                const float dn = c + 1 < nchunks ? tab[chunk_len(kEx, cs + r, sp, n)] : 1.f;
+                const int r_next = c + 1 < nchunks ? chunk_len(kEx, cs + r, sp, n) : 0;
+                const float dn = c + 1 >= nchunks ? 1.f : r_next == C ? dn_full : tab[r_next];
 #pragma unroll 1
                 for (int sub = 0; sub < 2; ++sub) {
                     const int col0 = wg * 64 + sub * 32;
@@ -716,7 +730,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- out: o = gamma D^-0.5 Oint + Ointra -> bf16, 32 columns at a time
             if (!(ok = warp_wait_bar(&bars->o_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
-            const float gam = tabp[i + 1];
 #pragma unroll 1
             for (int sub = 0; sub < 2; ++sub) {
                 const int col0 = wg * 64 + sub * 32;
