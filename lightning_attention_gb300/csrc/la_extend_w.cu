@@ -75,9 +75,13 @@ using namespace sm100;
 constexpr int C = 128;              // chunk length in tokens
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kColWarps = kEpiWarps / 4;      // epilogue warps per TMEM lane quarter
+constexpr int kSubs = 4 / kColWarps;          // 32-column parts of the state and output passes
+constexpr int kKUnits = 16 / kEpiWarps;       // lambda-K units (32 rows x 32 columns) per warp
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kThreads = (kEpiWarps + 2) * 32;
+static_assert(kColWarps == 2 || kColWarps == 4, "epilogue warps: 8 or 16");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_A = 0;        // 128 columns: Q K^T (fp32), then P (bf16 hi + lo pairs)
 constexpr uint32_t TM_OI = 128;     // 128 columns: Q S
@@ -512,17 +516,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------------ epilogue warps
         const int q = warp & 3;            // TMEM lane quarter
-        const int wg = warp >> 2;          // 64-column half for the state and output passes
+        const int cw = warp >> 2;          // column slot for the state and output passes
+        const int col_base = cw * 32 * kSubs;  // columns col_base .. col_base + 32 kSubs - 1
         const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (S)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        // Work split of the chunk's first phase.  Every warp first scales two of the 16 lambda-K
-        // units (4 row groups x 4 column quarters), so that MMA4 can start early; then lane
-        // quarter q's P blocks 0 .. q: its two warps (q, q + 4) take the lower and upper part, and
-        // warp q + 4 zeroes the blocks above the diagonal.
-        const int pb0 = wg ? (q + 2) >> 1 : 0;
-        const int pb1 = wg ? q + 1 : (q + 2) >> 1;
-        const bool pz = wg == 1 && q < 3;
-        const int ku0 = 2 * warp;  // units ku0 and ku0 + 1
+        // Work split of the chunk's first phase.  Every warp first scales kKUnits of the 16
+        // lambda-K units (4 row groups x 4 column quarters), so that MMA4 can start early; then
+        // lane quarter q's P blocks 0 .. q, split over its warps, and the zero blocks above the
+        // diagonal.  With four warps per quarter, warp (q, cw) owns block cw: P if cw <= q, else
+        // zero; with two, warp q takes the lower blocks, warp q + 4 the upper ones and the zeros.
+        const int pb0 = kColWarps == 4 ? cw : (cw ? (q + 2) >> 1 : 0);
+        const int pb1 = kColWarps == 4 ? (cw <= q ? cw + 1 : cw) : (cw ? q + 1 : (q + 2) >> 1);
+        const int zb0 = kColWarps == 4 ? cw : q + 1;
+        const int zb1 = kColWarps == 4 ? (cw > q ? cw + 1 : cw) : (cw == 1 ? 4 : q + 1);
+        const int ku0 = kKUnits * warp;  // units ku0 .. ku0 + kKUnits - 1
 
         const float slope = p.slopes[h];
         for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
@@ -535,15 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
-        // this row's share of the pool state: columns 64 wg .. 64 wg + 63
+        // this row's share of the pool state: columns col_base .. col_base + 32 kSubs - 1
         float *gstate =
-            p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)(wg * 64);
+            p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col_base;
         {
             const int r0 = nchunks > 0 ? chunk_len(kEx, 0, sp, n) : 0;
             const float d0s = tab[r0];  // 1 when there is no chunk
 #pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
-                const int col0 = wg * 64 + sub * 32;
+            for (int sub = 0; sub < kSubs; ++sub) {
+                const int col0 = col_base + sub * 32;
                 float S[32];
                 if (split) {
                     // S = e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, from
@@ -590,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < 32; ++x) S[x] = 0.f;
                 }
                 if (kEx && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
-                store_state_split(s_hi, s_lo, i, wg, sub, S);
+                store_state_split(s_hi, s_lo, i, col0 >> 6, (col0 >> 5) & 1, S);
                 // TMEM holds e^{-s r_0} S_0, onto which MMA4 of chunk 0 accumulates
                 uint32_t w[32];
 #pragma unroll
@@ -613,9 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunk are slow while the MMAs stream their operands.
         const float gam = tabp[i + 1];     // gamma_i D^-0.5
         const float dn_full = tab[C];      // decay over a full chunk
-        LamSplitBf lam_full[2];            // lambda of this warp's two K units' rows, full chunk
+        LamSplitBf lam_full[kKUnits];      // lambda of this warp's K units' rows, full chunk
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < kKUnits; ++k)
             lam_full[k] = lam_split_bf16(tab[C - 1 - (((ku0 + k) >> 2) * 32 + lane)]);
         // P start factors e^{-s (i - 32 cb)} D^-0.5 of this warp's (at most two) blocks
         const float f_p0 = pb0 < pb1 ? tabp[i - 32 * pb0] : 0.f;
@@ -631,15 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // ---- lambda K as a bf16 pair hi (in place) + lo: this warp's units of (32-row group,
             // 32-column quarter)
-            // both units' loads are issued before either is converted, so the warp waits for
-            // one shared-memory round trip instead of two
+            // all units' loads are issued before any is converted, so the warp waits for one
+            // shared-memory round trip
             {
-                uint4 kbuf[2][4];
-                uint4 *krow[2];
-                uint4 *lrow[2];
-                int rr[2], h4[2];
+                uint4 kbuf[kKUnits][4];
+                uint4 *krow[kKUnits];
+                uint4 *lrow[kKUnits];
+                int rr[kKUnits], h4[kKUnits];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                for (int k = 0; k < kKUnits; ++k) {
                     const int u = ku0 + k;
                     rr[k] = (u >> 2) * 32 + lane;
                     const uint32_t roff = (u & 2) * 8192 + rr[k] * 128;
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ch = 0; ch < 4; ++ch) kbuf[k][ch] = krow[k][(h4[k] + ch + rr[k]) & 7];
                 }
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                for (int k = 0; k < kKUnits; ++k) {
                     const LamSplitBf lam = r == C ? lam_full[k]
                                                   : lam_split_bf16(rr[k] < r ? tab[r - 1 - rr[k]] : 0.f);
 #pragma unroll
@@ -680,11 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(ta + (uint32_t)cb * 32u, ph);
                     tmem_st16(ta + (uint32_t)cb * 32u + 16u, pl);
                 }
-                if (pz) {
+                if (zb0 < zb1) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) pk[x] = 0u;
-                    for (int cb = q + 1; cb < 4; ++cb) {
+                    for (int cb = zb0; cb < zb1; ++cb) {
                         tmem_st16(ta + (uint32_t)cb * 32u, pk);
                         tmem_st16(ta + (uint32_t)cb * 32u + 16u, pk);
                     }
@@ -703,8 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r_next = c + 1 < nchunks ? chunk_len(kEx, cs + r, sp, n) : 0;
                 const float dn = c + 1 >= nchunks ? 1.f : r_next == C ? dn_full : tab[r_next];
 #pragma unroll 1
-                for (int sub = 0; sub < 2; ++sub) {
-                    const int col0 = wg * 64 + sub * 32;
+                for (int sub = 0; sub < kSubs; ++sub) {
+                    const int col0 = col_base + sub * 32;
                     const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)col0;
                     uint32_t w[32];
                     tmem_ld32(t_s, w);
@@ -716,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w[x] = __float_as_uint(S[x] * dn);
                     }
                     tmem_st32(t_s, w);
-                    store_state_split(s_hi, s_lo, i, wg, sub, S);
+                    store_state_split(s_hi, s_lo, i, col0 >> 6, (col0 >> 5) & 1, S);
                     if (kEx && cs + r == sp)
                         store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
                 }
@@ -731,8 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->o_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
-                const int col0 = wg * 64 + sub * 32;
+            for (int sub = 0; sub < kSubs; ++sub) {
+                const int col0 = col_base + sub * 32;
                 uint32_t vi[32], vp[32];
                 tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)col0, vi);
                 tmem_ld32(tbase + lane_off + TM_OP + (uint32_t)col0, vp);
@@ -802,9 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // error word already reports the failure.  The last state pass left S unscaled.
         if (ok && !*abort_flag && last_seg) {
 #pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
+            for (int sub = 0; sub < kSubs; ++sub) {
                 uint32_t w[32];
-                tmem_ld32(tbase + lane_off + TM_S + (uint32_t)(wg * 64 + sub * 32), w);
+                tmem_ld32(tbase + lane_off + TM_S + (uint32_t)(col_base + sub * 32), w);
                 tmem_ld_wait_regs(w);
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
