@@ -120,6 +120,8 @@ def aggregate_throughput(units_per_rank_step: float, steps: int, world: int,
 # ----------------------------------------------------------------------------------------------
 # workload geometry: tokens and algorithmic HBM bytes / tensor flops per call
 
+CHUNK = 128  # the extend kernel's chunk length
+
 def algorithmic(w) -> dict:
     H = w.H
     if w.kind == "decode":
@@ -144,7 +146,9 @@ def algorithmic(w) -> dict:
         if w.track_lens is not None:
             byts += int((w.track_lens >= 0).sum()) * H * D * D * 4   # the snapshots
         flops = w.T * H * 4 * D * D           # the recurrence's own 4 d^2 per token-head
-        issued = None                         # filled from the kernel's chunk geometry
+        # what the tensor cores are given per token-head, C = 128: Q K^T 2Cd, then Q S, the state
+        # update and P V each as a bf16 hi + lo pair, 2 x 2d^2 + 2 x 2d^2 + 2 x 2Cd
+        issued = w.T * H * (6 * CHUNK * D + 8 * D * D)
     return {"tokens": tokens, "bytes": byts, "flops": flops, "issued_flops": issued}
 
 
@@ -374,9 +378,15 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
     tensor = None
     if w.kind == "extend":
         tflops = geo["flops"] / per_launch / 1e12
+        itflops = geo["issued_flops"] / per_launch / 1e12
         tensor = {"recurrence_tflops": round(tflops, 2),
                   "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
-                  "note": "4 d^2 flops per token-head (the recurrence's own count)"}
+                  "note": "4 d^2 flops per token-head (the recurrence's own count)",
+                  "issued_tflops": round(itflops, 2),
+                  "issued_frac_of_bf16_peak": round(itflops / peaks["bf16_tflops"], 4),
+                  "issued_note": "6 C d + 8 d^2 flops per token-head at C = 128: Q K^T, and Q S, "
+                                 "the state update and P V each as a bf16 hi + lo pair; the "
+                                 "time includes every launch of the call"}
 
     e2e = None
     if with_e2e:
