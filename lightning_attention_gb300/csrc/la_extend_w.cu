@@ -43,7 +43,9 @@
 //               read of a row happens in the warp that overwrites it); then, per 64-column half
 //               (warp / 4): the state pass (S to bf16 hi + lo in shared memory for MMA2, snapshot
 //               if tracked, S times the next chunk's decay back to TMEM) and the output pass
-//               (gamma D^-0.5 Oint + Ointra -> bf16 -> global).
+//               (gamma D^-0.5 Oint + Ointra -> bf16 -> global), after which Oint and Ointra are
+//               released to the next chunk's MMA2 and MMA3.  The per-row decay factors of full
+//               chunks are read from the table once, before the first chunk.
 // TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128.
 //
 // Per chunk c, the MMA thread issues MMA2_c (after the state pass of c-1 and the output pass of
