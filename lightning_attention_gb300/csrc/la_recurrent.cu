@@ -58,12 +58,16 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
 
     const int t_begin = MODE == RECUR_DECODE ? b : b * p.N;
     const int n = MODE == RECUR_DECODE ? 1 : p.N;
+    // Tree: the states that a later token forks from (bit t) are stored with the default cache
+    // policy so that the fork reloads them from L2; every other intermediate state is streamed.
+    unsigned long long reused = 0ull;
     if (MODE == RECUR_TREE) {
         // parents must point backwards; checked up front so that a bad tree writes nothing
         bool bad = false;
         for (int t = 0; t < n; ++t) {
             const int par = p.parents[(size_t)b * p.N + t];
             bad |= par < -1 || par >= t;
+            if (par >= 0 && par != t - 1 && par < 64) reused |= 1ull << par;
         }
         if (bad) {
             if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_PARENTS);
@@ -124,9 +128,16 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
         }
         if (MODE == RECUR_VERIFY || MODE == RECUR_TREE) {
             float *dst = p.inter + (((size_t)b * p.N + t) * H + h) * (size_t)(kHeadDim * kHeadDim);
+            if (MODE == RECUR_TREE && t < 64 && ((reused >> t) & 1ull)) {
 #pragma unroll
-            for (int r = 0; r < kRowsPerWarp; ++r)
-                __stcs(reinterpret_cast<float4 *>(dst + (size_t)(row0 + r) * kHeadDim + col), s[r]);
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    *reinterpret_cast<float4 *>(dst + (size_t)(row0 + r) * kHeadDim + col) = s[r];
+            } else {
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    __stcs(reinterpret_cast<float4 *>(dst + (size_t)(row0 + r) * kHeadDim + col),
+                           s[r]);
+            }
         }
         float(*buf)[kHeadDim] = red[t & 1];
         *reinterpret_cast<float4 *>(&buf[warp][col]) = o;
