@@ -105,9 +105,10 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *                overlap on the GPU.
  *   workspace_bytes  size of workspace
  *   stream       cudaStream_t
- * Numerics: bf16 inputs; fp32 states and accumulation; Q K^T runs on the tensor cores in bf16,
- * the state operand of Q S in two bf16 halves (hi + lo), P V and K^T V in fp16, all accumulating
- * in fp32; out is rounded to bf16 once.
+ * Numerics: bf16 inputs; fp32 states and accumulation.  Every product runs on the tensor cores
+ * in bf16 with fp32 accumulation, and the three operands the kernel computes -- the decay-masked
+ * scores P, the decayed keys lambda K and the state for Q S -- each as a bf16 pair hi + lo (about
+ * 2^-17 together); out is rounded to bf16 once.
  */
 la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
                     float *state_pool, int num_slots, const int32_t *state_idx,

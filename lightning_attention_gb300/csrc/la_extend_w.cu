@@ -492,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tbase + TM_S, dKlo + mnofs(kk), dV + mnofs(kk), idU, 1);
                 mma_commit(&bars->u_full);
                 mma_commit(&bars->k_empty[st]);
-                // Ointra = P V once P is in TMEM: it runs while the epilogue does the state pass
+                // Ointra = P_hi V + P_lo V once P is in TMEM: it runs while the epilogue does the
+                // state pass
                 if (!wait_bar(&bars->p_ready, c & 1, limit, abort_flag, p.err)) {
                     ok = false;
                     break;

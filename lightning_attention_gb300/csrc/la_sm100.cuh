@@ -9,7 +9,6 @@
 #pragma once
 
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace la {
@@ -156,13 +155,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            ((uint32_t)(M >> 4) << 24);
 }
 
-// Instruction descriptor for kind::f16 with fp16 A and B and an fp32 accumulator (A/B format 0).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle.
 // Bits: [0,14) start address >> 4, [16,30) leading-dimension byte offset >> 4,
 // [32,46) stride-dimension byte offset >> 4, [46,49) fixed 0b001, [61,64) swizzle (2 = 128B).
@@ -268,12 +260,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, uint32_t bloc
     const int c = (col & 63) >> 3;
     return (uint32_t)blk * block_stride + (uint32_t)row * 128u +
            ((uint32_t)(c ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
-}
-
-// Pack two floats into an fp16x2 word (round to nearest even), low half = a.
-__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
 }
 
 // Pack two floats into a bf16x2 word (round to nearest even), low half = a.
