@@ -310,30 +310,31 @@ class GpuCase:
             self.launches_per_step += 1
             self.kernel += " + commit_kernel"
 
-    def step(self, q=None, k=None, v=None, idx=None):
+    def step(self, q=None, k=None, v=None, idx=None, out=None):
         la, w = self.la, self.w
+        out = self.out if out is None else out
         q = self.q if q is None else q
         k = self.k if k is None else k
         v = self.v if v is None else v
         idx = self.idx if idx is None else idx
         if w.kind == "decode":
-            la.decode(q, k, v, self.slopes, self.pool, idx, out=self.out)
+            la.decode(q, k, v, self.slopes, self.pool, idx, out=out)
         elif w.kind == "verify":
             la.verify_chain(q, k, v, self.slopes, self.pool, idx, w.N,
-                            inter_states=self.inter, out=self.out)
+                            inter_states=self.inter, out=out)
             if self.accept is not None:
                 la.commit_accepted(self.inter, self.accept, self.pool, idx)
         elif w.kind == "tree":
             la.verify_tree(q, k, v, self.slopes, self.pool, idx, self.parents, w.N,
-                           inter_states=self.inter, out=self.out)
+                           inter_states=self.inter, out=out)
         elif self.track is not None:
-            la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=self.out,
+            la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=out,
                       max_seqlen=self.max_seqlen, track_lens=self.track[0],
                       track_state_idx=self.track[1])
         else:
-            la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=self.out,
+            la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=out,
                       max_seqlen=self.max_seqlen)
-        return self.out
+        return out
 
 
 def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sampler=None):
@@ -403,37 +404,62 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
 def time_e2e(case, w, geo, steps, world, dev):
     """Same metric through the public API with host buffers: per step, pinned-host -> device
     copies of the step's inputs (q, k, v, slot indices) and a device -> host read of the output,
-    all inside the timed region.  The state pool stays resident on the device."""
+    all inside the timed region, and the host waits for every step's result.  Steps are
+    pipelined as a serving loop would: inputs and outputs are double-buffered, the copies run on
+    their own streams, so step k+1's inputs travel while step k computes and step k's output
+    travels while step k+1 computes; the library calls stay in order on one stream (decode and
+    extend update the pool in place).  The state pool stays resident on the device."""
     hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
     hidx = w.state_idx.pin_memory()
-    hout = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
-    didx = torch.empty_like(case.idx)
+    houts = [torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory() for _ in range(2)]
+    dins = [(torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v),
+             torch.empty_like(case.idx)) for _ in range(2)]
+    douts = [torch.empty_like(case.out) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hidx))
-    d2h = hout.numel() * hout.element_size()
+    d2h = houts[0].numel() * houts[0].element_size()
     e2e_steps = max(1, min(steps, 50))
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    e_in, e_done, e_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def one():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        didx.copy_(hidx, non_blocking=True)
-        out = case.step(dq, dk, dv, didx)
-        hout.copy_(out, non_blocking=True)
+    def issue(n):
+        j = n & 1
+        dq, dk, dv, didx = dins[j]
+        with torch.cuda.stream(s_in):
+            if n >= 2:
+                s_in.wait_event(e_done[j])      # step n-2 is done with input buffers j
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            e_in[j].record(s_in)
+        comp.wait_event(e_in[j])
+        if n >= 2:
+            comp.wait_event(e_out[j])           # step n-2's output has left buffer j
+        case.step(dq, dk, dv, didx, out=douts[j])
+        e_done[j].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e_done[j])
+            houts[j].copy_(douts[j], non_blocking=True)
+            e_out[j].record(s_out)
 
-    one()
+    issue(0)
     torch.cuda.synchronize(dev)
     barrier(world, dev)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        one()
-        torch.cuda.current_stream(dev).synchronize()
+    for n in range(e2e_steps):
+        issue(n)
+        if n >= 1:
+            e_out[(n - 1) & 1].synchronize()    # the host reads step n-1's result
+    e_out[(e2e_steps - 1) & 1].synchronize()
     t1 = time.perf_counter()
+    torch.cuda.synchronize(dev)
     barrier(world, dev)
     max_s = max_over_ranks(t1 - t0, world, dev)
     return {"value": aggregate_throughput(geo["tokens"], e2e_steps, world, max_s),
             "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps}
+            "steps": e2e_steps, "pipelined": "copies on their own streams, double-buffered"}
 
 
 # ----------------------------------------------------------------------------------------------
