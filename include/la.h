@@ -286,6 +286,16 @@ const char *la_status_string(la_status status);
  */
 void la_set_wait_limit(uint64_t microseconds);
 
+/*
+ * la_set_column_split -- scheduling switch for la_extend / la_extend_ex (default 1: on).  When a
+ * call runs without a sequence split and its B * H CTAs leave at least H of the device's SMs
+ * idle, the longest requests (as many as the idle SMs allow, H CTAs each) run as two CTAs per
+ * head, each on one 64-column half of the values, which shortens the longest chunk chains.  The
+ * result is the same up to rounding either way.  0 runs one CTA per (request, head) always.
+ * Host only; applies to later launches from this process.
+ */
+void la_set_column_split(int enable);
+
 #ifdef __cplusplus
 }
 #endif

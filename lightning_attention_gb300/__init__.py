@@ -5,4 +5,5 @@ include/la.h; this package holds the ctypes binding (binding.py), the in-tree bu
 and the seeded synthetic workloads (workloads.py).
 """
 from .binding import (LAError, commit_accepted, decode, extend, extend_noalloc, extend_workspace_size, load,  # noqa
-                      poll_error, set_wait_limit, slopes, verify_chain, verify_tree)
+                      poll_error, set_column_split, set_wait_limit, slopes, verify_chain,
+                      verify_tree)

@@ -25,7 +25,7 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_C
 
 EXPORTS = ("la_slopes", "la_extend", "la_extend_ex", "la_extend_workspace_size", "la_decode",
            "la_verify_chain", "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
-           "la_set_wait_limit")
+           "la_set_wait_limit", "la_set_column_split")
 
 
 class LAError(RuntimeError):
@@ -78,6 +78,8 @@ def load():
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_set_wait_limit.argtypes = [ctypes.c_uint64]
         lib.la_set_wait_limit.restype = None
+        lib.la_set_column_split.argtypes = [ctypes.c_int]
+        lib.la_set_column_split.restype = None
         _lib = lib
         return lib
 
@@ -137,6 +139,12 @@ def slopes(H: int, layer_id: int, L: int) -> torch.Tensor:
 
 def set_wait_limit(polls: int) -> None:
     load().la_set_wait_limit(int(polls))
+
+
+def set_column_split(enable: bool) -> None:
+    """Scheduling switch of the extend calls (on by default): with SMs to spare, the longest
+    requests run as two CTAs per head, one per 64-column half of the values."""
+    load().la_set_column_split(1 if enable else 0)
 
 
 def poll_error(device=None) -> None:

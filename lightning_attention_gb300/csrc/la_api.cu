@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -25,6 +26,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 unsigned int *g_err_ptr[kMaxDevices] = {nullptr};
 std::atomic<unsigned long long> g_wait_limit{0};
+std::atomic<int> g_column_split{1};
 
 // Default bound on a device wait: far above any legitimate wait inside one CTA (microseconds),
 // short enough that a lost arrival ends the kernel in about two seconds instead of hanging.
@@ -95,6 +97,8 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out) {
 }
 
 void la_set_wait_limit(uint64_t microseconds) { g_wait_limit.store(microseconds); }
+
+void la_set_column_split(int enable) { g_column_split.store(enable ? 1 : 0); }
 
 la_status la_poll_error(la_stream stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -291,6 +295,15 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
             p.nblk = pl.nblk;
             p.ws = static_cast<float *>(workspace);
         }
+    }
+    // Column split: SMs that one CTA per (request, head) leaves idle take the second value-column
+    // half of the longest requests, H CTAs per request.
+    p.csplit = 0;
+    if (p.seg_len == 0 && T > 0 && g_column_split.load() && (B == 1 || p.lpt)) {
+        int sms = 0;
+        if ((st = num_sms(&sms)) != LA_OK) return st;
+        const long long spare = (long long)sms - (long long)B * H;
+        if (spare >= H) p.csplit = (int)std::min<long long>(B, spare / H);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.seg_len > 0) {

@@ -48,6 +48,14 @@
 //               chunks are read from the table once, before the first chunk.
 // TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128.
 //
+// Column split.  When one CTA per (request, head) leaves SMs idle, the longest requests run as two
+// CTAs per head, each on one 64-column half of the values (NV = 64): S[:, cols] and out[:, cols]
+// depend only on V[:, cols], so the halves share nothing.  A half repeats the lambda-K units, P
+// and MMA1 (they span all 128 key dimensions and keys) but runs MMA2, MMA4 and MMA3 with N = 64
+// and halves the state and output passes, so its chunks are shorter and the longest request's
+// chain no longer ends the kernel first.  The column count is a template parameter of the CTA's
+// code path.
+//
 // Per chunk c, the MMA thread issues MMA2_c (after the state pass of c-1 and the output pass of
 // c-1), MMA4_c (after K is scaled and V has landed), MMA3_c (after P), then MMA1_{c+1}.  The
 // orders that make the buffer reuse safe: MMA1_{c+1} overwrites A/P after MMA3_c by issue order;
@@ -78,12 +86,13 @@ constexpr int C = 128;              // chunk length in tokens
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kColWarps = kEpiWarps / 4;      // epilogue warps per TMEM lane quarter
-constexpr int kSubs = 4 / kColWarps;          // 32-column parts of the state and output passes
 constexpr int kKUnits = 16 / kEpiWarps;       // lambda-K units (32 rows x 32 columns) per warp
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kThreads = (kEpiWarps + 2) * 32;
-static_assert(kColWarps == 2 || kColWarps == 4, "epilogue warps: 8 or 16");
+// Two warps per lane quarter: each takes 32 of every 64 value columns in the state and output
+// passes, so a CTA that covers one 64-column half of the values (nv = 64) still splits evenly.
+static_assert(kColWarps == 2, "epilogue warps: 8");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_A = 0;        // 128 columns: Q K^T (fp32), then P (bf16 hi + lo pairs)
 constexpr uint32_t TM_OI = 128;     // 128 columns: Q S
@@ -269,44 +278,21 @@ __device__ __forceinline__ int chunk_len(bool ex, int cs, int sp, int n) {
     return min(C, (ex && cs < sp ? min(sp, n) : n) - cs);
 }
 
-// kEx: the options variant (state-tracking snapshots, caller-given output strides)
-template <bool kEx>
-__global__ void __launch_bounds__(kThreads, 1)
-    extend_wide_kernel(const __grid_constant__ CUtensorMap tq,
-                       const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const ExtendParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *sm = smem_raw + (base - raw);
+// One CTA's work: request b, head h, segment g, value columns c0 .. c0 + NV - 1 (NV = 128, or 64
+// under the column split).
+template <bool kEx, int NV>
+__device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensorMap &tk,
+                                           const CUtensorMap &tv, const ExtendParams &p,
+                                           uint8_t *sm, const int g, const int h, const int b,
+                                           const int c0_half) {
+    constexpr int nv = NV;                               // value columns of this CTA
+    const int c0 = NV == kHeadDim ? 0 : c0_half;         // its first value column
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     float *tab = reinterpret_cast<float *>(sm + OFF_TAB);
     float *tabp = reinterpret_cast<float *>(sm + OFF_TABP);
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int H = p.H;
-    const int g = blockIdx.x % p.nseg;  // segment of the request (0 when not split)
-    const int bh = blockIdx.x / p.nseg;
-    const int h = bh % H;
-    int b = bh / H;
-    if (p.lpt) {
-        // Longest request first: CTAs are issued in index order, so taking requests in
-        // decreasing length order (ties by index) keeps long requests from finishing last.
-        __shared__ int s_req;
-        const int want = b;
-        for (int t = threadIdx.x; t < p.B; t += kThreads) {
-            const int lt = p.cu_seqlens[t + 1] - p.cu_seqlens[t];
-            int rank = 0;
-            for (int u = 0; u < p.B; ++u) {
-                const int lu = p.cu_seqlens[u + 1] - p.cu_seqlens[u];
-                rank += (lu > lt) || (lu == lt && u < t);
-            }
-            if (rank == want) s_req = t;
-        }
-        __syncthreads();
-        b = s_req;
-    }
 
     // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
     const int slot = p.state_idx[b];
@@ -416,9 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q_issued = c + 1;
                 if (c >= 1 && !wait_bar(&bars->v_empty, (c - 1) & 1, limit, abort_flag, p.err))
                     break;
-                mbar_arrive_expect_tx(&bars->v_full, SZ_T);
-                tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq, y);
-                tma_load_2d(sm + OFF_V + 16384, &tv, &bars->v_full, xq + 64, y);
+                if constexpr (nv == kHeadDim) {
+                    mbar_arrive_expect_tx(&bars->v_full, SZ_T);
+                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq, y);
+                    tma_load_2d(sm + OFF_V + 16384, &tv, &bars->v_full, xq + 64, y);
+                } else {
+                    mbar_arrive_expect_tx(&bars->v_full, SZ_T / 2);
+                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq + c0, y);
+                }
                 v_issued = c + 1;
             }
             // Copies still in flight must land before the CTA's shared memory goes away.
@@ -434,9 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idA = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t idI = idesc_bf16_f32(128, 128, false, true);
-            const uint32_t idP = idesc_bf16_f32(128, 128, false, true);
-            const uint32_t idU = idesc_bf16_f32(128, 128, true, true);
+            // the products with V or S are nv columns wide
+            const uint32_t idI = idesc_bf16_f32(128, nv, false, true);
+            const uint32_t idP = idesc_bf16_f32(128, nv, false, true);
+            const uint32_t idU = idesc_bf16_f32(128, nv, true, true);
             const uint64_t dQ = sdesc_sw128(s_base + OFF_Q, 16, 1024);
             const uint64_t dK0 = sdesc_sw128(s_base + OFF_K, 16, 1024);
             const uint64_t dKt0 = sdesc_sw128(s_base + OFF_K, 16384, 1024);
@@ -520,18 +512,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ epilogue warps
         const int q = warp & 3;            // TMEM lane quarter
         const int cw = warp >> 2;          // column slot for the state and output passes
-        const int col_base = cw * 32 * kSubs;  // columns col_base .. col_base + 32 kSubs - 1
+        constexpr int nsubs = nv / (32 * kColWarps);  // 32-column parts per warp: 2, or 1 at nv = 64
+        const int col_base = cw * 32 * nsubs;  // columns col_base .. col_base + 32 nsubs - 1 of
+                                               // the CTA's nv (value column c0 + col)
         const int i = q * 32 + lane;       // row: token of the chunk (A, O) or k-dim (S)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         // Work split of the chunk's first phase.  Every warp first scales kKUnits of the 16
         // lambda-K units (4 row groups x 4 column quarters), so that MMA4 can start early; then
-        // lane quarter q's P blocks 0 .. q, split over its warps, and the zero blocks above the
-        // diagonal.  With four warps per quarter, warp (q, cw) owns block cw: P if cw <= q, else
-        // zero; with two, warp q takes the lower blocks, warp q + 4 the upper ones and the zeros.
-        const int pb0 = kColWarps == 4 ? cw : (cw ? (q + 2) >> 1 : 0);
-        const int pb1 = kColWarps == 4 ? (cw <= q ? cw + 1 : cw) : (cw ? q + 1 : (q + 2) >> 1);
-        const int zb0 = kColWarps == 4 ? cw : q + 1;
-        const int zb1 = kColWarps == 4 ? (cw > q ? cw + 1 : cw) : (cw == 1 ? 4 : q + 1);
+        // lane quarter q's P blocks 0 .. q, split over its two warps (warp q the lower blocks,
+        // warp q + 4 the upper ones), and the zero blocks above the diagonal (warp q + 4).
+        const int pb0 = cw ? (q + 2) >> 1 : 0;
+        const int pb1 = cw ? q + 1 : (q + 2) >> 1;
+        const int zb0 = q + 1;
+        const int zb1 = cw == 1 ? 4 : q + 1;
         const int ku0 = kKUnits * warp;  // units ku0 .. ku0 + kKUnits - 1
 
         const float slope = p.slopes[h];
@@ -545,14 +538,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");  // tables
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
-        // this row's share of the pool state: columns col_base .. col_base + 32 kSubs - 1
-        float *gstate =
-            p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim + (size_t)col_base;
+        // this row's share of the pool state: value columns c0 + col_base .. + 32 nsubs - 1
+        float *gstate = p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim +
+                        (size_t)(c0 + col_base);
         {
             const int r0 = nchunks > 0 ? chunk_len(kEx, 0, sp, n) : 0;
             const float d0s = tab[r0];  // 1 when there is no chunk
 #pragma unroll 1
-            for (int sub = 0; sub < kSubs; ++sub) {
+            for (int sub = 0; sub < nsubs; ++sub) {
                 const int col0 = col_base + sub * 32;
                 float S[32];
                 if (split) {
@@ -560,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the workspace the block-state kernel filled.
                     const float *w0 = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) *
                                                  (kHeadDim * kHeadDim) +
-                                      (size_t)i * kHeadDim + col0;
+                                      (size_t)i * kHeadDim + c0 + col0;
                     const float d0 = expf(-slope * (float)g * (float)p.seg_len);
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
@@ -599,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int x = 0; x < 32; ++x) S[x] = 0.f;
                 }
-                if (kEx && sp == 0) store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
+                if (kEx && sp == 0)
+                    store_state_row(p.pool, p.track_idx[b], H, h, i, c0 + col0, S);
                 store_state_split(s_hi, s_lo, i, col0 >> 6, (col0 >> 5) & 1, S);
                 // TMEM holds e^{-s r_0} S_0, onto which MMA4 of chunk 0 accumulates
                 uint32_t w[32];
@@ -713,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r_next = c + 1 < nchunks ? chunk_len(kEx, cs + r, sp, n) : 0;
                 const float dn = c + 1 >= nchunks ? 1.f : r_next == C ? dn_full : tab[r_next];
 #pragma unroll 1
-                for (int sub = 0; sub < kSubs; ++sub) {
+                for (int sub = 0; sub < nsubs; ++sub) {
                     const int col0 = col_base + sub * 32;
                     const uint32_t t_s = tbase + lane_off + TM_S + (uint32_t)col0;
                     uint32_t w[32];
@@ -728,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(t_s, w);
                     store_state_split(s_hi, s_lo, i, col0 >> 6, (col0 >> 5) & 1, S);
                     if (kEx && cs + r == sp)
-                        store_state_row(p.pool, p.track_idx[b], H, h, i, col0, S);
+                        store_state_row(p.pool, p.track_idx[b], H, h, i, c0 + col0, S);
                 }
                 tmem_st_wait();
             }
@@ -741,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->o_full, c & 1, limit, abort_flag, p.err))) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int sub = 0; sub < kSubs; ++sub) {
+            for (int sub = 0; sub < nsubs; ++sub) {
                 const int col0 = col_base + sub * 32;
                 uint32_t vi[32], vp[32];
                 tmem_ld32(tbase + lane_off + TM_OI + (uint32_t)col0, vi);
@@ -799,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int row = rbase + k;
                     if (row < r) {
                         __nv_bfloat16 *dst = p.out + (size_t)(t0 + cs + row) * row_stride +
-                                             (size_t)h * head_stride + col0 + pq * 8;
+                                             (size_t)h * head_stride + c0 + col0 + pq * 8;
                         *reinterpret_cast<uint4 *>(dst) = ch[k];
                     }
                 }
@@ -812,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // error word already reports the failure.  The last state pass left S unscaled.
         if (ok && !*abort_flag && last_seg) {
 #pragma unroll 1
-            for (int sub = 0; sub < kSubs; ++sub) {
+            for (int sub = 0; sub < nsubs; ++sub) {
                 uint32_t w[32];
                 tmem_ld32(tbase + lane_off + TM_S + (uint32_t)(col_base + sub * 32), w);
                 tmem_ld_wait_regs(w);
@@ -832,6 +826,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tmem_dealloc(tbase, kTmemCols);
     }
+}
+
+// kEx: the options variant (state-tracking snapshots, caller-given output strides)
+template <bool kEx>
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_wide_kernel(const __grid_constant__ CUtensorMap tq,
+                       const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const ExtendParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+
+    const int H = p.H;
+    const int g = blockIdx.x % p.nseg;  // segment of the request (0 when not split)
+    const int bh = blockIdx.x / p.nseg;
+    int h = bh % H;
+    int want = bh / H;  // the request's rank in decreasing length order when p.lpt is set
+    // Column split: the p.csplit longest requests run as two CTAs per head, each on one 64-column
+    // half of the values (CTAs 2 (rank H + h) + half), the other requests as one CTA per head.
+    // The halves share nothing: S[:, cols] depends only on V[:, cols].
+    int half = -1;
+    if (p.csplit > 0) {
+        const int x = blockIdx.x;  // no sequence split alongside
+        if (x < 2 * p.csplit * H) {
+            want = x / (2 * H);
+            h = (x >> 1) % H;
+            half = x & 1;
+        } else {
+            const int y = x - p.csplit * H;
+            want = y / H;
+            h = y % H;
+        }
+    }
+    int b = want;
+    if (p.lpt) {
+        // Longest request first: CTAs are issued in index order, so taking requests in
+        // decreasing length order (ties by index) keeps long requests from finishing last.
+        __shared__ int s_req;
+        for (int t = threadIdx.x; t < p.B; t += kThreads) {
+            const int lt = p.cu_seqlens[t + 1] - p.cu_seqlens[t];
+            int rank = 0;
+            for (int u = 0; u < p.B; ++u) {
+                const int lu = p.cu_seqlens[u + 1] - p.cu_seqlens[u];
+                rank += (lu > lt) || (lu == lt && u < t);
+            }
+            if (rank == want) s_req = t;
+        }
+        __syncthreads();
+        b = s_req;
+    }
+
+
+    // The value-column count is a compile-time constant of each CTA's code path.
+    if (half < 0)
+        extend_cta<kEx, kHeadDim>(tq, tk, tv, p, sm, g, h, b, 0);
+    else
+        extend_cta<kEx, kHeadDim / 2>(tq, tk, tv, p, sm, g, h, b, half * (kHeadDim / 2));
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -873,7 +925,8 @@ bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H) {
 }
 
 cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream) {
-    const long long units = (long long)p.B * p.H * (p.seg_len > 0 ? p.nseg : 1);
+    const long long units =
+        (long long)p.B * p.H * (p.seg_len > 0 ? p.nseg : 1) + (long long)p.csplit * p.H;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap tq, tk, tv;

@@ -72,6 +72,10 @@ struct ExtendParams {
     int nblk;      // blocks per request kept in the workspace
     float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
+    // Column split (0: none; only without a sequence split).  The csplit longest requests run as
+    // two CTAs per head, one per 64-column half of the values, which shortens their chunk chains
+    // when the batch leaves SMs idle; the grid has (B + csplit) H CTAs.
+    int csplit;
     // State tracking (both null: none).  For b with track_lens[b] >= 0 the state after the first
     // track_lens[b] tokens of the request is also written to slot track_idx[b]; the CTA that
     // holds that token restarts its chunk grid there and stores the state at that boundary.
