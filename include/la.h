@@ -99,10 +99,12 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *   workspace    device scratch of workspace_bytes bytes (16-byte aligned), or NULL.  When the
  *                batch has too few (request, head) pairs to fill the GPU, long requests are cut
  *                into segments processed in parallel; that needs la_extend_workspace_size()
- *                bytes of scratch.  With NULL or a smaller buffer the call runs unsplit (same
- *                results up to rounding, fewer CTAs).  The caller owns it; its contents on entry
- *                do not matter and are garbage on exit; calls sharing one workspace must not
- *                overlap on the GPU.
+ *                bytes of scratch.  With NULL or a smaller buffer the call runs without that
+ *                split (same results up to rounding, fewer CTAs).  The caller owns it; its
+ *                contents on entry do not matter and are garbage on exit; calls sharing one
+ *                workspace must not overlap on the GPU.  Without the sequence split, SMs left
+ *                idle may take the longest requests as two CTAs per head (la_set_column_split);
+ *                that needs no scratch.
  *   workspace_bytes  size of workspace
  *   stream       cudaStream_t
  * Numerics: bf16 inputs; fp32 states and accumulation.  Every product runs on the tensor cores

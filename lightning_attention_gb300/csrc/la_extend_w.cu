@@ -34,19 +34,20 @@
 //               once the previous chunk's products with them are done;
 //   warp 9      TMEM allocator and MMA issuer (one thread), all bf16 with fp32 accumulation:
 //                 MMA1  A       = Q K^T                            -> TMEM (128 columns)
-//                 MMA2  Oint    = Q S_hi + Q S_lo                  -> TMEM (128 columns)
+//                 MMA2  Oint    = Q S_hi + Q S_lo                  -> TMEM (NV columns)
 //                 MMA4  S      += (lambda K)_hi^T V + (lambda K)_lo^T V   -> TMEM (the state)
-//                 MMA3  Ointra  = P_hi V + P_lo V  (P from TMEM)   -> TMEM (128 columns)
+//                 MMA3  Ointra  = P_hi V + P_lo V  (P from TMEM)   -> TMEM (NV columns)
 //   warps 0-7   first phase: two units of lambda K each (32 rows x 32 columns; hi in place, lo
 //               into its own buffer), then the P blocks of their TMEM lane quarter (warp % 4):
 //               P = A o Dm D^-0.5 for 32 keys as hi + lo over that block's 32 columns of A (every
-//               read of a row happens in the warp that overwrites it); then, per 64-column half
-//               (warp / 4): the state pass (S to bf16 hi + lo in shared memory for MMA2, snapshot
+//               read of a row happens in the warp that overwrites it); then, per half of the
+//               CTA's NV value columns (warp / 4): the state pass (S to bf16 hi + lo in shared memory for MMA2, snapshot
 //               if tracked, S times the next chunk's decay back to TMEM) and the output pass
 //               (gamma D^-0.5 Oint + Ointra -> bf16 -> global), after which Oint and Ointra are
 //               released to the next chunk's MMA2 and MMA3.  The per-row decay factors of full
 //               chunks are read from the table once, before the first chunk.
-// TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128.
+// TMEM (512 columns): A / P 128, Oint 128, Ointra 128, S 128 (NV = 128 value columns; a CTA of
+// the column split below uses the first 64 of Oint, Ointra and S).
 //
 // Column split.  When one CTA per (request, head) leaves SMs idle, the longest requests run as two
 // CTAs per head, each on one 64-column half of the values (NV = 64): S[:, cols] and out[:, cols]
