@@ -1,8 +1,10 @@
 """Seeded random extend calls that combine the options: ragged lengths (with zero-length requests and
 lengths on both sides of chunk edges), 1-4 heads, caller-given slopes from 0 to 3 (log-uniform
 over six decades, plus exact zeros), random prefix flags, state-tracking snapshots at random
-offsets (including 0 and the full length), and the three output layouts.  Every case is compared
-with the fp64 oracle on outputs, final states, snapshots, and on the slots no request names.
+offsets (including 0 and the full length), and the three output layouts.  Even seeds run with the
+column split (two CTAs per head, one per value-column half, for the requests that idle SMs can
+take), odd seeds without it.  Every case is compared with the fp64 oracle on outputs, final
+states, snapshots, and on the slots no request names.
 """
 import numpy as np
 import pytest
@@ -31,8 +33,15 @@ def draw_case(seed):
     return rng, lengths, H, slopes.astype(np.float32), prefix, track, layout
 
 
+@pytest.fixture
+def column_split():
+    yield la.set_column_split
+    la.set_column_split(True)
+
+
 @pytest.mark.parametrize("seed", range(24))
-def test_extend_fuzz(seed):
+def test_extend_fuzz(seed, column_split):
+    column_split(seed % 2 == 0)
     rng, lengths, H, slopes, prefix, track, layout = draw_case(seed)
     B = len(lengths)
     w = workloads.custom_extend(lengths, H=H, prefix=prefix, num_slots=2 * B + 2, seed=seed)
@@ -73,7 +82,7 @@ def test_extend_fuzz(seed):
         o_ref, p_ref = oracle.extend(qn, kn, vn, s64, pool0.double().numpy(), w.state_idx.numpy(),
                                      w.cu_seqlens.numpy(), w.prefix_mask.numpy(), H, 128)
     got = to64(view.reshape(T, H * 128))  # a copy in token-major order for the strided view
-    tag = f"seed {seed} (B={B} H={H} lengths={lengths} track={track} {layout})"
+    tag = f"seed {seed} (B={B} H={H} lengths={lengths} track={track} {layout} split={seed % 2 == 0})"
     assert_close(got, o_ref, f"{tag}: out")
     written = set(int(x) for x in w.state_idx.numpy())
     if track:
