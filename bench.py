@@ -47,12 +47,13 @@ D = 128
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# Which source file holds each workload's dominant kernel (used to invalidate stored ncu traffic).
+# Which source files hold the kernels a workload's step launches (used to invalidate stored ncu
+# traffic).
 KERNEL_SOURCE = {
     "decode": "la_recurrent.cu",
     "verify": "la_recurrent.cu",
     "varlen_extend": "la_extend_w.cu",
-    "long_prefill": "la_extend_w.cu",
+    "long_prefill": ("la_extend_w.cu", "la_extend_seg.cu"),
     "verify_tree": "la_recurrent.cu",
     "varlen_extend_tracked": "la_extend_w.cu",
     "verify_commit": "la_recurrent.cu",
@@ -169,11 +170,12 @@ def read_peaks():
                 "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
 
 
-def source_digest(fname: str) -> str:
-    """Digest of a kernel's source file and the local headers it includes (recursively)."""
+def source_digest(fname) -> str:
+    """Digest of a kernel source file (or a tuple of them) and the local headers they include
+    (recursively)."""
     csrc = os.path.join(ROOT, "lightning_attention_gb300", "csrc")
     h = hashlib.sha256()
-    seen, todo = set(), [fname]
+    seen, todo = set(), [fname] if isinstance(fname, str) else list(fname)
     while todo:
         name = todo.pop(0)
         if name in seen:
