@@ -376,8 +376,7 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
             "traffic": stored_traffic(name), "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": geo["bytes"], "kernel": case.kernel,
             "launch_ms": round(per_launch * 1e3, 4)}
-    if case.launches_per_step > 1:
-        roof["traffic"] = None  # ncu traffic is recorded for single-kernel calls only
+    # for a step of two launches (long prefill, verify + commit) the stored traffic covers both
     tensor = None
     if w.kind == "extend":
         tflops = geo["flops"] / per_launch / 1e12
