@@ -22,8 +22,10 @@
  *   - Only head_dim D = 128 is supported (LA_ERR_UNSUPPORTED otherwise), in the spirit of the
  *     head-dim entry guards the page's section "输入与配置覆盖" describes.  q, k and v share one
  *     head count H (no grouped-query heads), as the same section states for seg_la.
- *   - Device pointers to q, k, v, out and state_pool must be 16-byte aligned (the extend kernel
- *     moves them with TMA and 16-byte vector accesses); LA_ERR_INVALID otherwise.
+ *   - Device pointers to q, k, v, out, state_pool and inter_states must be 16-byte aligned (the
+ *     kernels move them with TMA and 16-byte vector accesses), and the fp32 and int32 arrays
+ *     (slopes, state_idx, cu_seqlens, parents, accept_idx, track arrays) 4-byte aligned; a call
+ *     given a misaligned pointer returns LA_ERR_INVALID before anything is launched.
  *   - Pointers marked "device" must be device memory of the current CUDA device (or managed
  *     memory); "host" pointers are host memory.  The caller owns every buffer; the library keeps
  *     no pointer after a call returns and allocates no device memory.
@@ -33,10 +35,11 @@
  *     Faults the host cannot see (a slot index out of range, inconsistent cu_seqlens, a device
  *     wait that ran out) are recorded in a per-device error word and reported by la_poll_error.
  *   - Preconditions the host cannot check: the state_idx entries of one call are distinct and lie
- *     in [0, num_slots); cu_seqlens is non-decreasing, starts at 0 and ends at T; out overlaps no
- *     input; inputs are finite.  Out-of-range slots and inconsistent cu_seqlens are detected on
- *     the device (the affected request is skipped and the error word set); duplicate slots and
- *     overlapping buffers give undefined results.
+ *     in [0, num_slots); cu_seqlens is non-decreasing, starts at 0 and ends at T; no request is
+ *     longer than max_seqlen; out overlaps no input; inputs are finite.  Out-of-range slots,
+ *     inconsistent cu_seqlens and requests longer than max_seqlen are detected on the device
+ *     (the affected request is skipped -- nothing of it is written -- and the error word set);
+ *     duplicate slots and overlapping buffers give undefined results.
  *   - Argument errors (NULL pointers with B > 0, negative sizes, H < 1, num_slots < 1 ...) return
  *     LA_ERR_INVALID before anything is launched.  B = 0 is a no-op returning LA_OK.
  */
@@ -56,8 +59,9 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,  /* valid but unsupported configuration (head_dim != 128, ...) */
     LA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     LA_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (reported by la_poll_error) */
-    LA_ERR_DEVICE_INPUT = 5  /* the device found an index out of range: a slot, cu_seqlens, a tree
-                                parent, an accept or a track entry (reported by la_poll_error) */
+    LA_ERR_DEVICE_INPUT = 5  /* the device found an index out of range: a slot, cu_seqlens, a
+                                request longer than max_seqlen, a tree parent, an accept or a
+                                track entry (reported by la_poll_error) */
 } la_status;
 
 typedef uint16_t la_bf16; /* bfloat16 bit pattern */
@@ -95,8 +99,12 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *   out          device, bf16 [T][H*D], written
  *   B, T, H, D   requests, total tokens (= cu_seqlens[B]), heads, head_dim (must be 128)
  *   max_seqlen   an upper bound on every request's length (T is always a valid value); it and
- *                B, H decide the schedule (see la_extend_workspace_size)
- *   workspace    device scratch of workspace_bytes bytes (16-byte aligned), or NULL.  When the
+ *                B, H decide the schedule (see la_extend_workspace_size).  A request longer than
+ *                max_seqlen is skipped (no output rows, no state written) and la_poll_error
+ *                reports LA_ERR_DEVICE_INPUT.
+ *   workspace    device scratch of workspace_bytes bytes (16-byte aligned), or NULL.  (This
+ *                argument pair extends the plain call with a caller-owned scratch buffer, so
+ *                that the library itself never allocates.)  When the
  *                batch has too few (request, head) pairs to fill the GPU, long requests are cut
  *                into segments processed in parallel; that needs la_extend_workspace_size()
  *                bytes of scratch.  With NULL or a smaller buffer the call runs without that
@@ -179,10 +187,12 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
  * keeps in device memory on every device that loads it (held until the process exits).
  *   - It allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  *   - A batch whose split plan needs more than 16 MiB of scratch is rejected with
- *     LA_ERR_UNSUPPORTED before anything is launched (on a 152-SM GB300 every plan fits; use
- *     la_extend with a workspace otherwise).
+ *     LA_ERR_UNSUPPORTED before anything is launched.  The largest plan is 1.5 x (SM count)
+ *     matrices of 64 KiB -- 14.25 MiB on a 152-SM GB300 -- so every plan fits on devices of up to
+ *     170 SMs; use la_extend with a workspace otherwise.
  *   - The first call on a device looks up the array's device address and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  Do not use it again in a process after
+ *     cudaDeviceReset (the cached address belongs to the old context).
  *   - All calls on a device share the array and it keeps the last call's contents; nothing in it
  *     needs to start at zero, but calls that overlap on the GPU race on it: serialise them.
  */
@@ -211,8 +221,8 @@ la_status la_decode(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
 /*
  * la_verify_chain -- chain (topk = 1) target verify of N draft tokens per request.
  * [LA-page §生产环境不支持, item 3]: seg_la treats draft tokens as a chain, each one continuing
- * from the previous position's state; tree verify is not supported (the page's backend refuses
- * topk > 1), and neither is it here.  For each request b and head h, from
+ * from the previous position's state (the page's backend refuses topk > 1; la_verify_tree below
+ * is this library's tree variant).  For each request b and head h, from
  * S = state_pool[state_idx[b], h], for t = 0..N-1: apply the recurrence to token b*N + t, write
  * its output row, and store S into inter_states[b][t][h].  The pool is only read; committing an
  * accepted draft state is the caller's copy from inter_states.
@@ -267,11 +277,15 @@ la_status la_commit_accepted(const float *inter_states, const int32_t *accept_id
                              int N, int H, int D, la_stream stream);
 
 /*
- * la_poll_error -- synchronise `stream`, then read and clear the current device's error word.
- * Returns LA_ERR_TIMEOUT if a bounded device wait ran out, LA_ERR_DEVICE_INPUT if a kernel found
- * a slot index out of range, inconsistent cu_seqlens, a tree parent, commit index or track entry
- * out of range, LA_ERR_CUDA if the stream reports a CUDA error, else LA_OK.  This is the one call
- * that blocks the host.
+ * la_poll_error -- synchronise `stream` and then the whole current device (every stream on it),
+ * then read and clear the device's error word.  The word is shared by all of the library's
+ * kernels on the device, whatever stream they run on, so the device-wide synchronisation makes
+ * sure that a fault recorded by a kernel still running on another stream is neither missed nor
+ * reported by a later poll.  Returns LA_ERR_TIMEOUT if a bounded device wait ran out,
+ * LA_ERR_DEVICE_INPUT if a kernel found a slot index out of range, inconsistent cu_seqlens, a
+ * request longer than max_seqlen, a tree parent, commit index or track entry out of range,
+ * LA_ERR_CUDA if a CUDA error is pending, else LA_OK.  This is the one call that blocks the host
+ * (and it cannot be captured in a CUDA graph).
  */
 la_status la_poll_error(la_stream stream);
 

@@ -33,6 +33,8 @@ std::atomic<int> g_column_split{1};
 constexpr unsigned long long kDefaultWaitLimitUs = 2000000ull;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// int32, fp32 and uint8 arrays are read element by element: 4-byte alignment (1 for uint8)
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 la_status error_word_ptr(unsigned int **out) {
     int dev = 0;
@@ -101,8 +103,12 @@ void la_set_wait_limit(uint64_t microseconds) { g_wait_limit.store(microseconds)
 void la_set_column_split(int enable) { g_column_split.store(enable ? 1 : 0); }
 
 la_status la_poll_error(la_stream stream) {
+    // The error word is per device, so every kernel that may write it -- on any stream of the
+    // device -- has to be finished before it is read: synchronise the stream given (which may
+    // belong to another context's default) and then the whole device.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     unsigned int *err = nullptr;
     la_status st = error_word_ptr(&err);
@@ -129,6 +135,10 @@ la_status la_decode(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
     if (B == 0) return LA_OK;
     if (!q || !k || !v || !slopes || !state_pool || !state_idx || !out) return LA_ERR_INVALID;
+    // the kernel moves q, k, v, the states and out with 16-byte vector accesses
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_pool) ||
+        !aligned16(out) || !aligned4(slopes) || !aligned4(state_idx))
+        return LA_ERR_INVALID;
     la::RecurParams p{};
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
@@ -155,6 +165,9 @@ la_status la_verify_chain(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     if ((long long)B * N > 0x7fffffffLL) return LA_ERR_INVALID;
     if (B == 0) return LA_OK;
     if (!q || !k || !v || !slopes || !state_pool || !state_idx || !inter_states || !out)
+        return LA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_pool) ||
+        !aligned16(inter_states) || !aligned16(out) || !aligned4(slopes) || !aligned4(state_idx))
         return LA_ERR_INVALID;
     la::RecurParams p{};
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
@@ -184,6 +197,10 @@ la_status la_verify_tree(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v,
     if (B == 0) return LA_OK;
     if (!q || !k || !v || !slopes || !state_pool || !state_idx || !parents || !inter_states || !out)
         return LA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_pool) ||
+        !aligned16(inter_states) || !aligned16(out) || !aligned4(slopes) || !aligned4(state_idx) ||
+        !aligned4(parents))
+        return LA_ERR_INVALID;
     la::RecurParams p{};
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
@@ -210,7 +227,9 @@ la_status la_commit_accepted(const float *inter_states, const int32_t *accept_id
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
     if (B == 0) return LA_OK;
     if (!inter_states || !accept_idx || !state_pool || !state_idx) return LA_ERR_INVALID;
-    if (!aligned16(inter_states) || !aligned16(state_pool)) return LA_ERR_INVALID;
+    if (!aligned16(inter_states) || !aligned16(state_pool) || !aligned4(accept_idx) ||
+        !aligned4(state_idx))
+        return LA_ERR_INVALID;
     la::CommitParams p{};
     p.inter = inter_states;
     p.accept_idx = accept_idx;
@@ -254,6 +273,9 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     if ((long long)T * H * D >= (1ll << 40)) return LA_ERR_UNSUPPORTED;
     if (!aligned16(state_pool) || (T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
                                              !aligned16(out))))
+        return LA_ERR_INVALID;
+    if (!aligned4(slopes) || !aligned4(state_idx) || !aligned4(cu_seqlens) ||
+        (track_lens && (!aligned4(track_lens) || !aligned4(track_state_idx))))
         return LA_ERR_INVALID;
     la_status st;
     la::ExtendParams p{};

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (slot < 0 || slot >= p.num_slots || t0 < 0 || t1 < t0 || t1 > p.T) return;  // the extend
     // kernel, launched next on the same stream, records these faults in the error word
     const int n = t1 - t0;
+    if (n > p.max_seqlen) return;  // longer than the caller's bound: reported by the extend kernel
     const int nseg_b = (n + p.seg_len - 1) / p.seg_len;
     if (nseg_b <= 1) return;  // not split
     const int per_seg = p.seg_len / p.blk_len;

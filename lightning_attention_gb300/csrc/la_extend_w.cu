@@ -309,6 +309,12 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
     }
     // Segment [t0, t1) of the request: the whole request unless long requests are split.
     const int n_req = t_req1 - t_req0;
+    // max_seqlen is the caller's bound on every request's length, and the split schedule has no
+    // CTA for the segments past it: a longer request is reported and skipped, never half-written.
+    if (n_req > p.max_seqlen) {
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, ERR_BIT_SEQLENS);
+        return;
+    }
     int nseg_b = 1, t0 = t_req0, t1 = t_req1;
     if (p.seg_len > 0) {
         nseg_b = n_req > 0 ? (n_req + p.seg_len - 1) / p.seg_len : 1;

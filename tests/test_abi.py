@@ -105,6 +105,49 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.la_commit_accepted(n, n, n, 1, n, 0, 1, 1, 128, n) == 0
 
 
+def test_misaligned_pointers_are_refused_before_any_launch(lib):
+    """Every pointer the kernels move with 16-byte accesses must be 16-byte aligned, and the int32
+    and fp32 arrays 4-byte aligned: a misaligned one returns LA_ERR_INVALID on the host, so it can
+    never become a misaligned-address fault on the device.  (Each call below has one misaligned
+    pointer and is refused before any CUDA call, so it runs the same with or without a GPU.)"""
+    ct = ctypes
+    ok, bad16, bad4 = ct.c_void_p(4096), ct.c_void_p(4096 + 8), ct.c_void_p(4096 + 2)
+
+    def decode(q=ok, k=ok, v=ok, s=ok, pool=ok, idx=ok, out=ok):
+        return lib.la_decode(q, k, v, s, pool, 4, idx, out, 1, 1, 128, None)
+
+    for kw in ({"q": bad16}, {"k": bad16}, {"v": bad16}, {"pool": bad16}, {"out": bad16},
+               {"s": bad4}, {"idx": bad4}):
+        assert decode(**kw) == 1, kw
+
+    def chain(q=ok, k=ok, v=ok, s=ok, pool=ok, idx=ok, inter=ok, out=ok):
+        return lib.la_verify_chain(q, k, v, s, pool, 4, idx, inter, out, 1, 2, 1, 128, None)
+
+    for kw in ({"q": bad16}, {"k": bad16}, {"v": bad16}, {"pool": bad16}, {"inter": bad16},
+               {"out": bad16}, {"s": bad4}, {"idx": bad4}):
+        assert chain(**kw) == 1, kw
+
+    def tree(q=ok, k=ok, v=ok, s=ok, pool=ok, idx=ok, par=ok, inter=ok, out=ok):
+        return lib.la_verify_tree(q, k, v, s, pool, 4, idx, par, inter, out, 1, 2, 1, 128, None)
+
+    for kw in ({"q": bad16}, {"k": bad16}, {"v": bad16}, {"pool": bad16}, {"inter": bad16},
+               {"out": bad16}, {"s": bad4}, {"idx": bad4}, {"par": bad4}):
+        assert tree(**kw) == 1, kw
+
+    def extend(q=ok, k=ok, v=ok, s=ok, pool=ok, idx=ok, cu=ok, pm=ok, out=ok):
+        return lib.la_extend(q, k, v, s, pool, 4, idx, cu, pm, out, 1, 8, 1, 128, 8, None, 0, None)
+
+    for kw in ({"q": bad16}, {"k": bad16}, {"v": bad16}, {"pool": bad16}, {"out": bad16},
+               {"s": bad4}, {"idx": bad4}, {"cu": bad4}):
+        assert extend(**kw) == 1, kw
+
+    def commit(inter=ok, acc=ok, pool=ok, idx=ok):
+        return lib.la_commit_accepted(inter, acc, pool, 4, idx, 1, 2, 1, 128, None)
+
+    for kw in ({"inter": bad16}, {"pool": bad16}, {"acc": bad4}, {"idx": bad4}):
+        assert commit(**kw) == 1, kw
+
+
 def test_status_strings(lib):
     for code, name in binding.STATUS.items():
         assert lib.la_status_string(code).decode().startswith(name)

@@ -135,6 +135,42 @@ def test_bad_cu_seqlens_is_reported():
     assert e.value.status == 5
 
 
+@pytest.mark.parametrize("lengths,H,max_seqlen", [
+    ([100, 300], 2, 200),          # one CTA per (request, head): no split
+    ([8192, 2048], 16, 4096),      # the split schedule (block states in the workspace)
+])
+def test_request_longer_than_max_seqlen_is_reported_not_written(lengths, H, max_seqlen):
+    """max_seqlen is the caller's bound on every request's length.  A longer request is skipped
+    -- no output row, no state written -- and reported as LA_ERR_DEVICE_INPUT; the requests
+    within the bound are computed as usual."""
+    w = workloads.custom_extend(lengths, H=H, prefix=[1] * len(lengths), seed=41)
+    pool0 = w.materialize_pool()
+    pool = pool0.to(DEV)
+    out = torch.full((w.T, H * 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(H, 0, 1).to(DEV), pool,
+              w.state_idx.to(DEV), w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV), out=out,
+              max_seqlen=max_seqlen)
+    with pytest.raises(la.LAError) as e:
+        la.poll_error()
+    assert e.value.status == 5
+    la.poll_error()  # cleared
+    cu = w.cu_seqlens.numpy()
+    o_ref, p_ref = oracle.extend(w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy(),
+                                 oracle_slopes_fp32(H, 0, 1), pool0.double().numpy(),
+                                 w.state_idx.numpy(), cu, w.prefix_mask.numpy(), H, 128)
+    out_h, pool_h = out.cpu(), pool.cpu()
+    for b, n in enumerate(lengths):
+        rows = slice(int(cu[b]), int(cu[b + 1]))
+        slot = int(w.state_idx[b])
+        if n > max_seqlen:
+            assert (out_h[rows] == 7.0).all(), f"request {b} wrote output rows"
+            assert torch.equal(pool_h[slot].view(torch.int32), pool0[slot].view(torch.int32)), \
+                f"request {b} wrote its state"
+        else:
+            assert_close(to64(out_h[rows]), o_ref[rows], f"request {b}: out")
+            assert_close(pool_h[slot].double().numpy(), p_ref[slot], f"request {b}: state")
+
+
 def test_verify_small_and_decode_identity():
     """Verify outputs and states equal successive decodes from the same pool state."""
     w = workloads.custom_verify(3, 4, H=2, seed=4)
