@@ -9,6 +9,7 @@ If the compiled library is missing or cannot be loaded, every call raises: there
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -91,11 +92,30 @@ def _check(func: str, status: int):
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # the arguments are declared c_void_p, so ctypes takes the integer address as is
+    return None if t is None else t.data_ptr()
+
+
+# The current stream's raw handle without building a torch.cuda.Stream object per call (the
+# public route below is the fallback); a decode call is short enough that the binding's own
+# per-call cost shows up next to the kernel.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream_handle(device: torch.device):
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if _raw_stream is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+_NO_SWITCH = contextlib.nullcontext()
+
+
+def _on(device: torch.device):
+    """Make `device` current for the library call; no switch when it already is."""
+    if torch.cuda.current_device() == device.index:
+        return _NO_SWITCH
+    return torch.cuda.device(device)
 
 
 def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
@@ -137,8 +157,10 @@ def slopes(H: int, layer_id: int, L: int) -> torch.Tensor:
     return torch.tensor(list(out)[:H], dtype=torch.float32)
 
 
-def set_wait_limit(polls: int) -> None:
-    load().la_set_wait_limit(int(polls))
+def set_wait_limit(microseconds: int) -> None:
+    """Bound (in microseconds) on every device wait inside the extend kernels; 0 restores the
+    default of two seconds (la_set_wait_limit)."""
+    load().la_set_wait_limit(int(microseconds))
 
 
 def set_column_split(enable: bool) -> None:
@@ -150,7 +172,7 @@ def set_column_split(enable: bool) -> None:
 def poll_error(device=None) -> None:
     """Synchronise the current stream and raise if a kernel recorded a device-side fault."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    _check("la_poll_error", load().la_poll_error(_stream_handle(dev)))
+    _check("la_poll_error", load().la_poll_error(ctypes.c_void_p(_stream_handle(dev))))
 
 
 _ws_cache: dict = {}
@@ -212,7 +234,7 @@ def extend(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out
     if track_lens is not None:
         _need(track_lens, "track_lens", torch.int32, dev, (B,))
         _need(track_state_idx, "track_state_idx", torch.int32, dev, (B,))
-    with torch.cuda.device(dev):
+    with _on(dev):
         if workspace is None:
             nbytes = extend_workspace_size(B, T, H, D, int(max_seqlen))
             ws = _cached_workspace(dev, nbytes) if nbytes > 0 else None
@@ -268,7 +290,7 @@ def extend_noalloc(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_m
     _need(out, "out", torch.bfloat16, dev, (T, H * D))
     if max_seqlen is None:
         max_seqlen = T
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib.la_extend_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                    num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),
                                    _ptr(out), B, T, H, D, int(max_seqlen), _stream_handle(dev))
@@ -289,7 +311,7 @@ def decode(q, k, v, slopes_, state_pool, state_idx, out=None):
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, dev, (B, H * D))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().la_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool), num_slots,
                               _ptr(state_idx), _ptr(out), B, H, D, _stream_handle(dev))
     _check("la_decode", st)
@@ -313,7 +335,7 @@ def verify_chain(q, k, v, slopes_, state_pool, state_idx, N: int, inter_states=N
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, dev, (B * N, H * D))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().la_verify_chain(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                     num_slots, _ptr(state_idx), _ptr(inter_states), _ptr(out), B,
                                     N, H, D, _stream_handle(dev))
@@ -340,7 +362,7 @@ def verify_tree(q, k, v, slopes_, state_pool, state_idx, parents, N: int, inter_
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, dev, (B * N, H * D))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().la_verify_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
                                    num_slots, _ptr(state_idx), _ptr(parents), _ptr(inter_states),
                                    _ptr(out), B, N, H, D, _stream_handle(dev))
@@ -358,7 +380,7 @@ def commit_accepted(inter_states, accept_idx, state_pool, state_idx):
     _need(accept_idx, "accept_idx", torch.int32, dev, (B,))
     _need(state_pool, "state_pool", torch.float32, dev)
     _need(state_idx, "state_idx", torch.int32, dev, (B,))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().la_commit_accepted(_ptr(inter_states), _ptr(accept_idx), _ptr(state_pool),
                                        num_slots, _ptr(state_idx), B, N, H, D, _stream_handle(dev))
     _check("la_commit_accepted", st)
