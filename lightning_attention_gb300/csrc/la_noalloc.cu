@@ -11,11 +11,14 @@
 //
 // Facts a caller needs:
 //   * The array is kNoAllocScratchBytes (16 MiB) on every device that loads this library, held
-//     until the process exits.  On a 152-SM GB300 every split plan fits (the planner never asks
-//     for more than about 14.3 MiB); a plan that needs more is rejected with LA_ERR_UNSUPPORTED and
-//     nothing is launched.
+//     until the process exits.  The split planner asks for at most 1.5 x (number of SMs) fp32
+//     128 x 128 matrices of 64 KiB (one request whose head count is half the SM count), i.e.
+//     14.25 MiB on a 152-SM GB300, so every plan fits on any device of up to 170 SMs.  A plan
+//     that needs more is rejected with LA_ERR_UNSUPPORTED and nothing is launched.
 //   * The first call on a device looks the array's device address up (cudaGetSymbolAddress, with
-//     that device current) and caches it; make that first call before any stream capture.
+//     that device current) and caches it; make that first call before any stream capture.  The
+//     cached address belongs to the device's current context: after cudaDeviceReset the module is
+//     loaded anew, so do not call this entry point again in that process.
 //   * Every call on a device shares the one array, and it keeps the last call's contents.  Nothing
 //     in it has to start at zero: each call writes every value it later reads (the initial-state
 //     copy and the block states) before reading it.  Calls that overlap on the GPU (for example on
