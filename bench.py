@@ -18,8 +18,14 @@ Every workload's inputs exceed the 129 MB L2, so no flush is needed between step
 data path); timing is bracketed by a barrier and the slowest rank's time is reported.
 
 The default run prints ONE JSON line for the decode workload and, unless --headline-only, adds
-the other workloads under "other_workloads" (each measured the same way).  `--impl reference`
-times the fp64 CPU oracle instead, on a bounded sample of the same workload.
+the other workloads under "other_workloads" (each timed the same way, three times over, with its
+own clock record, end-to-end rate and oracle baseline).  `--impl reference` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+
+Timing: after the warm-up, a barrier and a synchronize, one untimed lead step is enqueued and then
+the CUDA start event, the K timed steps and the end event, so that the GPU is already busy when
+the timed region opens (the host's enqueue of the first timed call would otherwise count as
+device time).  The host time spent enqueueing the K calls is reported per call.
 """
 from __future__ import annotations
 
@@ -339,7 +345,30 @@ class GpuCase:
         return out
 
 
-def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sampler=None):
+def timed_region(case, steps, world, dev, stream):
+    """Device time of exactly `steps` steps between CUDA events on the launching stream, with a
+    barrier and a synchronize on both sides.  One untimed lead step is enqueued after the
+    synchronize and before the first event, so that the GPU is busy when the timed region opens
+    and the host's enqueue of the first timed call is not counted as device time.  Returns
+    (device seconds, host seconds spent enqueueing the timed calls)."""
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    case.step()  # the lead step (untimed)
+    ev0.record(stream)
+    h0 = time.perf_counter()
+    for _ in range(steps):
+        case.step()
+    h1 = time.perf_counter()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    return ev0.elapsed_time(ev1) / 1e3, h1 - h0
+
+
+def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sampler=None,
+             repeats=1):
     import lightning_attention_gb300 as la
     w = make_workload(name, rank_seed(0, rank))
     geo = algorithmic(w)
@@ -349,26 +378,25 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
         case.step()
     la.poll_error()
 
-    barrier(world, dev)
-    torch.cuda.synchronize(dev)
     if sampler:
         sampler.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    ev0.record(stream)
-    for _ in range(steps):
-        case.step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    runs = [timed_region(case, steps, world, dev, stream) for _ in range(repeats)]
     wall1 = time.perf_counter()
-    barrier(world, dev)
     clocks = sampler.stop() if sampler else None
     la.poll_error()
-    dev_s = ev0.elapsed_time(ev1) / 1e3
+    # the reported run is the median one (the first when there is one); the others give the spread
+    order = sorted(range(repeats), key=lambda i: runs[i][0])
+    dev_s, host_s = runs[order[(repeats - 1) // 2]]
     max_s = max_over_ranks(dev_s, world, dev)
     per_launch = dev_s / steps  # one la_extend / la_decode / la_verify_chain call per step
     value = aggregate_throughput(geo["tokens"], steps, world, max_s)
+    spread = None
+    if repeats > 1:
+        ms = sorted(r[0] / steps * 1e3 for r in runs)
+        spread = {"repeats": repeats, "steps_each": steps, "ms_per_step_min": round(ms[0], 4),
+                  "ms_per_step_median": round(ms[(repeats - 1) // 2], 4),
+                  "ms_per_step_max": round(ms[-1], 4)}
 
     achieved_gbs = geo["bytes"] / per_launch / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
@@ -395,8 +423,9 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
         e2e = time_e2e(case, w, geo, steps, world, dev)
     res = {"value": value, "ms_per_step": max_s / steps * 1e3, "tokens_per_step": geo["tokens"],
            "gpu_launches": steps * case.launches_per_step,
+           "host_enqueue_us_per_call": round(host_s / steps * 1e6, 2),
            "roofline": roof, "wall_s": wall1 - wall0, "clocks": clocks, "e2e": e2e,
-           "workload": w, "geo": geo}
+           "workload": w, "geo": geo, "spread": spread}
     if tensor:
         res["tensor"] = tensor
     return res
@@ -564,10 +593,16 @@ ORACLE_BUDGET = {  # (request, head) pairs or token-heads per sample: ~1-10 s of
 
 
 def cpu_baseline(name, w, threads):
+    """The oracle as it stands on all host cores, and on one thread (on a quarter of the sample,
+    so that the single-thread leg stays within seconds)."""
     sample = oracle_sample(w, ORACLE_BUDGET[name])
     secs = run_oracle_sample(w, sample, threads)
+    single = oracle_sample(w, max(1, ORACLE_BUDGET[name] // 4))
+    secs1 = run_oracle_sample(w, single, 1)
     return {"value": sample["tokens"] / secs, "unit": "tokens/s", "cores": threads,
-            "kind": "oracle", "sample": sample["desc"], "seconds": round(secs, 3)}
+            "kind": "oracle", "sample": sample["desc"], "seconds": round(secs, 3),
+            "single_thread": {"value": single["tokens"] / secs1, "cores": 1,
+                              "sample": single["desc"], "seconds": round(secs1, 3)}}
 
 
 def cpu_model() -> str:
@@ -637,11 +672,12 @@ def main():
             "data": "synthetic (seeded; see lightning_attention_gb300/workloads.py)",
             "config": workload_config(args.workload, w, world),
             "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+            "host_enqueue_us_per_call": head["host_enqueue_us_per_call"],
             "clocks": head["clocks"]}
     if "tensor" in head:
         line["tensor"] = head["tensor"]
+    threads = os.cpu_count() or 1
     if rank == 0:
-        threads = os.cpu_count() or 1
         line["cpu_baseline"] = cpu_baseline(args.workload, w, threads)
         line["cpu_baseline"]["cpu"] = cpu_model()
     del head, w
@@ -649,18 +685,15 @@ def main():
 
     if not args.headline_only:
         others = []
-        for name in KERNEL_SOURCE:
+        for name in OTHER_ORDER:
             if name == args.workload:
                 continue
             steps = max(3, min(args.steps, 20))
+            smp = ClockSampler(local) if rank == 0 else None
             r = time_gpu(name, steps, max(3, args.warmup), world, rank, dev, peaks,
-                         with_e2e=False, sampler=None)
-            entry = {"workload": r["workload"].name, "value": r["value"], "unit": "tokens/s",
-                     "steps": steps, "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
-                     "gpu_launches": r["gpu_launches"]}
-            if "tensor" in r:
-                entry["tensor"] = r["tensor"]
-            others.append(entry)
+                         with_e2e=True, sampler=smp, repeats=3)
+            others.append(compact_entry(r, steps, cpu_baseline(name, r["workload"], threads)
+                                        if rank == 0 else None))
             del r
             torch.cuda.empty_cache()
         line["other_workloads"] = others
@@ -668,6 +701,42 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# The other workloads, each timed like the headline (3 repeats of up to 20 steps, clocks sampled
+# over them).  The chain verify of 128 x 5 draft tokens comes last so that it is in the tail of
+# the printed line.
+OTHER_ORDER = ("verify_tree", "varlen_extend_tracked", "verify_commit", "varlen_extend",
+               "long_prefill", "verify")
+
+
+def compact_entry(r, steps, cpu):
+    roof = r["roofline"]
+    e = {"workload": r["workload"].name, "value": r["value"], "unit": "tokens/s",
+         "steps": steps, "ms_per_step": round(r["ms_per_step"], 4), "spread": r["spread"],
+         "roofline": {"bound": roof["bound"], "achieved": roof["achieved"], "peak": roof["peak"],
+                      "unit": roof["unit"], "frac": roof["frac"], "traffic": roof["traffic"],
+                      "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
+                      "kernel": roof["kernel"]},
+         "gpu_launches": r["gpu_launches"],
+         "host_enqueue_us_per_call": r["host_enqueue_us_per_call"]}
+    if r.get("clocks"):
+        c = r["clocks"]
+        e["clocks"] = {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
+                       "reasons": c.get("reasons")}
+    if r.get("e2e"):
+        x = r["e2e"]
+        e["e2e"] = {"value": x["value"], "unit": x["unit"],
+                    "h2d_bytes_per_step": x["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": x["d2h_bytes_per_step"]}
+    if "tensor" in r:
+        t = r["tensor"]
+        e["tensor"] = {"recurrence_frac_of_bf16_peak": t["frac_of_bf16_peak"],
+                       "issued_frac_of_bf16_peak": t["issued_frac_of_bf16_peak"]}
+    if cpu is not None:
+        e["cpu_baseline"] = {"value": cpu["value"], "cores": cpu["cores"], "kind": "oracle",
+                             "single_thread_value": cpu["single_thread"]["value"]}
+    return e
 
 
 def main_profile(args):
