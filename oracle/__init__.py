@@ -62,6 +62,10 @@ def _bind(lib):
     lib.la_oracle_extend_tracked.restype = ci
     lib.la_oracle_commit_accepted.argtypes = [dp, ip, dp, ip, ci, ci, ci, ci]
     lib.la_oracle_commit_accepted.restype = ci
+    lib.la_oracle_extend_gqa.argtypes = [dp, dp, dp, dp, dp, ip, ip, up, dp, ci, ci, ci, ci, ci]
+    lib.la_oracle_extend_gqa.restype = ci
+    lib.la_oracle_decode_gqa.argtypes = [dp, dp, dp, dp, dp, ip, dp, ci, ci, ci, ci, ci]
+    lib.la_oracle_decode_gqa.restype = ci
     return lib
 
 
@@ -236,3 +240,51 @@ def commit_accepted(inter, accept_idx, pool, state_idx, lib=None) -> np.ndarray:
     if rc != 0:
         raise ValueError("accept_idx must satisfy -1 <= accept_idx[b] < N")
     return pool_c
+
+
+def extend_gqa(q, k, v, slopes_, pool, state_idx, cu_seqlens, prefix_mask, H: int, Hkv: int,
+               D: int, nthreads: int | None = None, lib=None):
+    """Packed varlen extend with grouped-query heads: q [T, H*D], k and v [T, Hkv*D], slopes
+    [Hkv], pool [S, Hkv, D, D] (a float64 copy is updated and returned); query head h reads the
+    state of kv head h // (H // Hkv).  Returns (out [T, H*D], pool_after)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T = q.shape[0]
+    assert q.shape == (T, H * D) and k.shape == (T, Hkv * D) and v.shape == k.shape
+    s = _f64(slopes_)
+    assert s.shape == (Hkv,)
+    pool_c = _f64(pool).copy()
+    assert pool_c.shape[1:] == (Hkv, D, D)
+    idx = _i32(state_idx)
+    cu = _i32(cu_seqlens)
+    pm = np.ascontiguousarray(np.asarray(prefix_mask, dtype=np.uint8))
+    B = idx.shape[0]
+    assert cu.shape == (B + 1,) and pm.shape == (B,)
+    out = np.zeros((T, H * D), dtype=np.float64)
+    rc = (lib or _load()).la_oracle_extend_gqa(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+        _ptr(s, ctypes.c_double), _ptr(pool_c, ctypes.c_double), _ptr(idx, ctypes.c_int32),
+        _ptr(cu, ctypes.c_int32), _ptr(pm, ctypes.c_uint8), _ptr(out, ctypes.c_double),
+        B, H, Hkv, D, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("H must be a positive multiple of Hkv")
+    return out, pool_c
+
+
+def decode_gqa(q, k, v, slopes_, pool, state_idx, H: int, Hkv: int, D: int,
+               nthreads: int | None = None, lib=None):
+    """One decode token per request with grouped-query heads: q [B, H*D], k and v [B, Hkv*D],
+    slopes [Hkv], pool [S, Hkv, D, D].  Returns (out [B, H*D], pool_after)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    s = _f64(slopes_)
+    pool_c = _f64(pool).copy()
+    idx = _i32(state_idx)
+    B = idx.shape[0]
+    assert q.shape == (B, H * D) and k.shape == (B, Hkv * D) and v.shape == k.shape
+    out = np.zeros((B, H * D), dtype=np.float64)
+    rc = (lib or _load()).la_oracle_decode_gqa(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+        _ptr(s, ctypes.c_double), _ptr(pool_c, ctypes.c_double), _ptr(idx, ctypes.c_int32),
+        _ptr(out, ctypes.c_double), B, H, Hkv, D, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("H must be a positive multiple of Hkv")
+    return out, pool_c

@@ -38,7 +38,13 @@
  *     not be the request's own slot;
  *   - chain verify leaves the pool untouched and records the state after each draft token;
  *   - tree verify: parent[t] in [-1, t-1], -1 meaning the request's pool state; the state after
- *     token t is the recurrence applied to token t from the state after its parent.
+ *     token t is the recurrence applied to token t from the state after its parent;
+ *   - grouped-query heads (a widening the page's section "输入与配置覆盖" says seg_la lacks: it
+ *     takes one head count for q, k and v): with H query heads and Hkv key/value heads (H a
+ *     multiple of Hkv, G = H / Hkv), query head h belongs to kv head j = h / G.  The state is a
+ *     property of the key/value stream, so there is one state and one slope per kv head: S^(j)
+ *     follows the page's recurrence with k^(j), v^(j) and slope_j, and every query head of the
+ *     group reads the same S^(j) out.  With Hkv = H this is the plain recurrence.
  *
  * Threads: the (request, head) pairs are independent, so they are spread over POSIX threads.
  * This changes no arithmetic: every pair is still one plain sequential loop.
@@ -296,6 +302,133 @@ int la_oracle_verify_chain(const double *q, const double *k, const double *v,
     a.state_idx = state_idx; a.inter = inter; a.out = out;
     a.B = B; a.H = H; a.D = D; a.N = N; a.nthreads = nthreads;
     return run(&a);
+}
+
+/* ---------------------------------------------------------------- grouped-query heads
+ * One kv head's recurrence over n tokens from S (in place), read out by its G query heads.
+ * qg, og point at the group's first query head of the first token (query head g at + g*D);
+ * kj, vj at the kv head's slice of the first token.  Per token the state is advanced once and
+ * then read out once per query head. */
+static void recur_group(double *S, int D, double slope, int n, int G, const double *qg,
+                        size_t q_stride, const double *kj, const double *vj, size_t kv_stride,
+                        double *og)
+{
+    const double decay = exp(-slope);
+    const double scale = 1.0 / sqrt((double)D);
+    for (int t = 0; t < n; t++) {
+        const double *kt = kj + (size_t)t * kv_stride;
+        const double *vt = vj + (size_t)t * kv_stride;
+        /* state_t = state_{t-1} * exp(-slope_j) + outer(k_t, v_t), once per kv head */
+        for (int i = 0; i < D; i++)
+            for (int j = 0; j < D; j++)
+                S[(size_t)i * D + j] = S[(size_t)i * D + j] * decay + kt[i] * vt[j];
+        /* o_t^(h) = q_t^(h) @ state_t * head_dim^-0.5 for each query head of the group */
+        for (int g = 0; g < G; g++) {
+            const double *qt = qg + (size_t)t * q_stride + (size_t)g * D;
+            double *ot = og + (size_t)t * q_stride + (size_t)g * D;
+            for (int j = 0; j < D; j++) {
+                double acc = 0.0;
+                for (int i = 0; i < D; i++)
+                    acc += qt[i] * S[(size_t)i * D + j];
+                ot[j] = acc * scale;
+            }
+        }
+    }
+}
+
+typedef struct {
+    int decode;
+    const double *q, *k, *v, *slopes;
+    double *pool;                 /* [num_slots][Hkv][D][D] */
+    const int32_t *state_idx, *cu_seqlens;
+    const uint8_t *prefix_mask;
+    double *out;                  /* [rows][H*D] */
+    int B, H, Hkv, D, nthreads, tid;
+} gqa_job_t;
+
+static void *gqa_worker(void *p)
+{
+    const gqa_job_t *a = (const gqa_job_t *)p;
+    const int D = a->D, G = a->H / a->Hkv;
+    const size_t q_row = (size_t)a->H * D, kv_row = (size_t)a->Hkv * D, dd = (size_t)D * D;
+    double *S = (double *)malloc(sizeof(double) * dd);
+    for (int w = a->tid; w < a->B * a->Hkv; w += a->nthreads) {
+        const int b = w / a->Hkv, j = w % a->Hkv;
+        double *slot = a->pool + ((size_t)a->state_idx[b] * a->Hkv + j) * dd;
+        int t0, n;
+        if (a->decode) {
+            t0 = b;
+            n = 1;
+            memcpy(S, slot, sizeof(double) * dd);
+        } else {
+            t0 = a->cu_seqlens[b];
+            n = a->cu_seqlens[b + 1] - t0;
+            if (a->prefix_mask[b])
+                memcpy(S, slot, sizeof(double) * dd);
+            else
+                memset(S, 0, sizeof(double) * dd);
+        }
+        const size_t qo = (size_t)t0 * q_row + (size_t)j * G * D;
+        const size_t kvo = (size_t)t0 * kv_row + (size_t)j * D;
+        recur_group(S, D, a->slopes[j], n, G, a->q + qo, q_row, a->k + kvo, a->v + kvo, kv_row,
+                    a->out + qo);
+        memcpy(slot, S, sizeof(double) * dd); /* final state of the kv head written back */
+    }
+    free(S);
+    return NULL;
+}
+
+static int run_gqa(gqa_job_t *a)
+{
+    if (a->Hkv < 1 || a->H < 1 || a->H % a->Hkv != 0)
+        return -1;
+    int nt = a->nthreads < 1 ? 1 : a->nthreads;
+    const int pairs = a->B * a->Hkv;
+    if (nt > pairs)
+        nt = pairs > 0 ? pairs : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nt);
+    gqa_job_t *jobs = (gqa_job_t *)malloc(sizeof(gqa_job_t) * nt);
+    for (int i = 0; i < nt; i++) {
+        jobs[i] = *a;
+        jobs[i].nthreads = nt;
+        jobs[i].tid = i;
+        if (nt == 1 || pthread_create(&th[i], NULL, gqa_worker, &jobs[i]) != 0) {
+            gqa_worker(&jobs[i]);
+            th[i] = 0;
+        }
+    }
+    for (int i = 0; i < nt; i++)
+        if (th[i])
+            pthread_join(th[i], NULL);
+    free(th);
+    free(jobs);
+    return 0;
+}
+
+/* Packed varlen extend with grouped-query heads: q, out are [T][H*D]; k, v are [T][Hkv*D];
+ * slopes [Hkv]; pool [num_slots][Hkv][D][D].  Returns -1 if H is not a multiple of Hkv. */
+int la_oracle_extend_gqa(const double *q, const double *k, const double *v, const double *slopes,
+                         double *pool, const int32_t *state_idx, const int32_t *cu_seqlens,
+                         const uint8_t *prefix_mask, double *out, int B, int H, int Hkv, int D,
+                         int nthreads)
+{
+    gqa_job_t a = {0};
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool;
+    a.state_idx = state_idx; a.cu_seqlens = cu_seqlens; a.prefix_mask = prefix_mask;
+    a.out = out; a.B = B; a.H = H; a.Hkv = Hkv; a.D = D; a.nthreads = nthreads;
+    return run_gqa(&a);
+}
+
+/* One-token decode with grouped-query heads: q, out [B][H*D]; k, v [B][Hkv*D]. */
+int la_oracle_decode_gqa(const double *q, const double *k, const double *v, const double *slopes,
+                         double *pool, const int32_t *state_idx, double *out, int B, int H,
+                         int Hkv, int D, int nthreads)
+{
+    gqa_job_t a = {0};
+    a.decode = 1;
+    a.q = q; a.k = k; a.v = v; a.slopes = slopes; a.pool = pool; a.state_idx = state_idx;
+    a.out = out; a.B = B; a.H = H; a.Hkv = Hkv; a.D = D; a.nthreads = nthreads;
+    return run_gqa(&a);
 }
 
 /* Accepted-state commit after a verify: for each request b with accept[b] >= 0, the pool slot

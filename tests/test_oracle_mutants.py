@@ -65,6 +65,23 @@ MUTANTS = {
                                    "memcpy(a->pool + ((size_t)a->state_idx[b] * H + h) * dd, S,"),
     "track_rest_not_processed": ("recur(S, D, a->slopes[h], n - n1, a->q + off2,",
                                  "recur(S, D, a->slopes[h], 0, a->q + off2,"),
+    # grouped-query heads
+    "gqa_kv_head_by_modulo": ("const size_t kvo = (size_t)t0 * kv_row + (size_t)j * D;",
+                              "const size_t kvo = (size_t)t0 * kv_row + (size_t)((j * G) % a->Hkv) * D;"),
+    "gqa_slope_of_query_head": ("recur_group(S, D, a->slopes[j], n, G,",
+                                "recur_group(S, D, a->slopes[(j * G) % a->Hkv], n, G,"),
+    "gqa_state_advanced_per_query_head": (
+        "        for (int g = 0; g < G; g++) {\n            const double *qt",
+        "        for (int g = 0; g < G; g++) {\n            if (g > 0)\n                for (int i = 0; i < D; i++)\n"
+        "                    for (int j = 0; j < D; j++)\n"
+        "                        S[(size_t)i * D + j] = S[(size_t)i * D + j] * decay + kt[i] * vt[j];\n"
+        "            const double *qt"),
+    "gqa_every_head_reads_the_first_query": ("const double *qt = qg + (size_t)t * q_stride + (size_t)g * D;",
+                                             "const double *qt = qg + (size_t)t * q_stride;"),
+    "gqa_group_offset_of_kv_head": ("const size_t qo = (size_t)t0 * q_row + (size_t)j * G * D;",
+                                    "const size_t qo = (size_t)t0 * q_row + (size_t)j * D;"),
+    "gqa_prefix_ignored": ("            if (a->prefix_mask[b])\n                memcpy(S, slot, sizeof(double) * dd);\n            else\n                memset(S, 0, sizeof(double) * dd);\n        }\n        const size_t qo",
+                           "            memset(S, 0, sizeof(double) * dd);\n        }\n        const size_t qo"),
 }
 
 

@@ -441,3 +441,95 @@ def test_tracking_rejects_bad_track_lengths_and_own_slot():
     ti[3] = idx[3]
     with pytest.raises(ValueError):
         oracle.extend_tracked(q, k, v, slopes, pool, idx, cu, pm, tls, ti, H, D)
+
+
+# ------------------------------------------------------------------ grouped-query heads
+# The page's seg_la takes one head count for q, k and v (section "输入与配置覆盖"); the grouped
+# variant lets H query heads share Hkv key/value heads, with one state and one slope per kv head.
+
+def _gqa_case(seed, H, Hkv, D, lens, num_slots=7):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((T, H * D))
+    k = r.standard_normal((T, Hkv * D))
+    v = r.standard_normal((T, Hkv * D))
+    slopes = r.uniform(0.01, 0.9, size=Hkv)
+    pool = r.standard_normal((num_slots, Hkv, D, D)) * 0.05
+    idx = r.permutation(num_slots)[:len(lens)].astype(np.int32)
+    pm = (np.arange(len(lens)) % 2 == 0).astype(np.uint8)
+    return q, k, v, slopes, pool, idx, cu, pm
+
+
+def test_gqa_closed_form_per_query_head():
+    """Every query head h reads the closed-form state of kv head h // G, from the same k, v and
+    slope; the kv head's final state is the closed-form end state."""
+    H, Hkv, D = 6, 2, 8
+    G = H // Hkv
+    lens = [7, 0, 12]
+    q, k, v, slopes, pool, idx, cu, pm = _gqa_case(21, H, Hkv, D, lens)
+    out, pool_after = oracle.extend_gqa(q, k, v, slopes, pool, idx, cu, pm, H, Hkv, D)
+    for b in range(len(lens)):
+        t0, t1 = cu[b], cu[b + 1]
+        for h in range(H):
+            j = h // G
+            sq, skv = slice(h * D, (h + 1) * D), slice(j * D, (j + 1) * D)
+            S0 = pool[idx[b], j] if pm[b] else np.zeros((D, D))
+            o_ref, S_ref = closed_form(q[t0:t1, sq], k[t0:t1, skv], v[t0:t1, skv], slopes[j], S0, D)
+            np.testing.assert_allclose(out[t0:t1, sq], o_ref, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(pool_after[idx[b], j], S_ref, rtol=1e-12, atol=1e-13)
+    untouched = np.setdiff1d(np.arange(pool.shape[0]), idx)
+    np.testing.assert_array_equal(pool_after[untouched], pool[untouched])
+
+
+def test_gqa_with_one_query_head_per_kv_head_is_the_plain_extend():
+    H = Hkv = 3
+    D = 8
+    q, k, v, slopes, pool, idx, cu, pm = _gqa_case(22, H, Hkv, D, [9, 4, 0, 17])
+    g_out, g_pool = oracle.extend_gqa(q, k, v, slopes, pool, idx, cu, pm, H, Hkv, D)
+    e_out, e_pool = oracle.extend(q, k, v, slopes, pool, idx, cu, pm, H, D)
+    np.testing.assert_array_equal(g_out, e_out)
+    np.testing.assert_array_equal(g_pool, e_pool)
+
+
+def test_gqa_group_equals_the_recurrence_with_the_kv_head_repeated():
+    """Repeating each kv head's k, v, slope and state G times turns the grouped call into the
+    plain per-head recurrence: same outputs, and every copy of a group's state ends equal to the
+    kv head's final state."""
+    H, Hkv, D = 8, 2, 8
+    G = H // Hkv
+    q, k, v, slopes, pool, idx, cu, pm = _gqa_case(23, H, Hkv, D, [11, 3, 20])
+    g_out, g_pool = oracle.extend_gqa(q, k, v, slopes, pool, idx, cu, pm, H, Hkv, D)
+    rep = np.repeat(np.arange(Hkv), G)
+    cols = np.concatenate([np.arange(j * D, (j + 1) * D) for j in rep])
+    e_out, e_pool = oracle.extend(q, k[:, cols], v[:, cols], slopes[rep], pool[:, rep], idx, cu,
+                                  pm, H, D)
+    np.testing.assert_array_equal(g_out, e_out)
+    for h in range(H):
+        np.testing.assert_array_equal(e_pool[idx][:, h], g_pool[idx][:, h // G])
+
+
+def test_gqa_decode_is_a_length_one_grouped_extend():
+    H, Hkv, D, B = 4, 2, 8, 5
+    q, k, v, slopes, pool, idx, _, _ = _gqa_case(24, H, Hkv, D, [1] * B, num_slots=9)
+    d_out, d_pool = oracle.decode_gqa(q, k, v, slopes, pool, idx, H, Hkv, D)
+    e_out, e_pool = oracle.extend_gqa(q, k, v, slopes, pool, idx,
+                                      np.arange(B + 1, dtype=np.int32), np.ones(B, np.uint8),
+                                      H, Hkv, D)
+    np.testing.assert_array_equal(d_out, e_out)
+    np.testing.assert_array_equal(d_pool, e_pool)
+    # one step in closed form: S' = e^-s_j S + k_j v_j^T, o_h = D^-0.5 q_h S'
+    G = H // Hkv
+    for b in range(B):
+        for h in range(H):
+            j = h // G
+            skv = slice(j * D, (j + 1) * D)
+            S1 = math.exp(-slopes[j]) * pool[idx[b], j] + np.outer(k[b, skv], v[b, skv])
+            np.testing.assert_allclose(d_out[b, h * D:(h + 1) * D], q[b, h * D:(h + 1) * D] @ S1
+                                       / math.sqrt(D), rtol=1e-12, atol=1e-14)
+
+
+def test_gqa_rejects_indivisible_heads():
+    q, k, v, slopes, pool, idx, cu, pm = _gqa_case(25, 4, 2, 8, [3])
+    with pytest.raises(ValueError):
+        oracle.extend_gqa(q[:, :3 * 8], k, v, slopes, pool, idx, cu, pm, 3, 2, 8)
