@@ -21,7 +21,8 @@
  *     outer(k, v)[i][j] = k_i v_j and (q @ S)[j] = sum_i q_i S[i][j].
  *   - Only head_dim D = 128 is supported (LA_ERR_UNSUPPORTED otherwise), in the spirit of the
  *     head-dim entry guards the page's section "输入与配置覆盖" describes.  q, k and v share one
- *     head count H (no grouped-query heads), as the same section states for seg_la.
+ *     head count H (no grouped-query heads), as the same section states for seg_la; the _gqa
+ *     entry points are the one widening of that, with their own head counts.
  *   - Device pointers to q, k, v, out, state_pool and inter_states must be 16-byte aligned (the
  *     kernels move them with TMA and 16-byte vector accesses), and the fp32 and int32 arrays
  *     (slopes, state_idx, cu_seqlens, parents, accept_idx, track arrays) 4-byte aligned; a call
@@ -201,6 +202,57 @@ la_status la_extend_noalloc(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v
                             const int32_t *state_idx, const int32_t *cu_seqlens,
                             const uint8_t *prefix_mask, la_bf16 *out, int B, int T, int H, int D,
                             int max_seqlen, la_stream stream);
+
+/*
+ * la_extend_gqa -- la_extend with grouped-query heads: H query heads share Hkv key/value heads.
+ * The page's section "输入与配置覆盖" notes that seg_la takes one head count for q, k and v (no
+ * grouped-query attention); this entry point is that widening, and la_extend stays the page's
+ * plain form.  The state is a property of the key/value stream, so there is one state and one
+ * slope per kv head: for request b and kv head j, S^(j) follows the recurrence of
+ * [LA-page §独立参考实现] with k^(j), v^(j) and slopes[j], and query head h of the group
+ * j = h / (H / Hkv) reads it out, o_t^(h) = (q_t^(h) @ S_t^(j)) * D^-0.5.  With Hkv = H this is
+ * la_extend, bit for bit.
+ *   q, out       device, bf16 [T][H*D]
+ *   k, v         device, bf16 [T][Hkv*D]
+ *   slopes       device, fp32 [Hkv]
+ *   state_pool   device, fp32 [num_slots][Hkv][D][D]
+ *   H, Hkv       query heads and kv heads; H must be a multiple of Hkv (LA_ERR_INVALID otherwise)
+ *   workspace    device scratch of at least la_extend_gqa_workspace_size() bytes when Hkv < H
+ *                (each kv head's initial state is copied there first, so that the group's first
+ *                query head can write the final state back while the others still start from
+ *                the copy); LA_ERR_INVALID when it is missing or smaller than the copies need.
+ *                The rest of the scratch, when present, lets long requests be split as in
+ *                la_extend.
+ * All other arguments, the checks and the errors are those of la_extend.  Each query head's CTA
+ * carries its kv head's state, so the kv-side work is repeated per query head; the K and V tiles
+ * the group's CTAs read at about the same time come from L2.
+ */
+la_status la_extend_gqa(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                        float *state_pool, int num_slots, const int32_t *state_idx,
+                        const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out,
+                        int B, int T, int H, int Hkv, int D, int max_seqlen, void *workspace,
+                        size_t workspace_bytes, la_stream stream);
+
+/*
+ * la_extend_gqa_workspace_size -- bytes of device scratch la_extend_gqa uses for a batch of this
+ * shape on the current device: the initial-state copies (B * Hkv matrices of D x D fp32) when
+ * Hkv < H, plus the split plan's block states when long requests are split; 0 when Hkv = H and
+ * nothing is split.  Host only.  LA_ERR_INVALID for bad sizes or bytes == NULL.
+ */
+la_status la_extend_gqa_workspace_size(int B, int T, int H, int Hkv, int D, int max_seqlen,
+                                       size_t *bytes);
+
+/*
+ * la_decode_gqa -- la_decode with grouped-query heads (see la_extend_gqa): one decode token per
+ * request; kv head j's state is advanced once, in place, and read out by each of its H / Hkv
+ * query heads.  One CTA per (request, kv head) does both, so a state crosses HBM once however
+ * many query heads share it.  q, out: device bf16 [B][H*D]; k, v: [B][Hkv*D]; slopes [Hkv];
+ * state_pool [num_slots][Hkv][D][D].  With Hkv = H this is la_decode.  Checks and errors as for
+ * la_decode; H must be a multiple of Hkv.
+ */
+la_status la_decode_gqa(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                        float *state_pool, int num_slots, const int32_t *state_idx, la_bf16 *out,
+                        int B, int H, int Hkv, int D, la_stream stream);
 
 /*
  * la_decode -- one decode token per request, state updated in place.

@@ -4,6 +4,7 @@ The computation runs in hand-written sm_103a CUDA kernels (csrc/), reached throu
 include/la.h; this package holds the ctypes binding (binding.py), the in-tree build (_build.py)
 and the seeded synthetic workloads (workloads.py).
 """
-from .binding import (LAError, commit_accepted, decode, extend, extend_noalloc, extend_workspace_size, load,  # noqa
+from .binding import (LAError, commit_accepted, decode, decode_gqa, extend, extend_gqa,  # noqa
+                      extend_gqa_workspace_size, extend_noalloc, extend_workspace_size, load,
                       poll_error, set_column_split, set_wait_limit, slopes, verify_chain,
                       verify_tree)

@@ -26,7 +26,8 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_C
 
 EXPORTS = ("la_slopes", "la_extend", "la_extend_ex", "la_extend_workspace_size", "la_decode",
            "la_verify_chain", "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
-           "la_set_wait_limit", "la_set_column_split")
+           "la_set_wait_limit", "la_set_column_split", "la_extend_noalloc", "la_extend_gqa",
+           "la_extend_gqa_workspace_size", "la_decode_gqa")
 
 
 class LAError(RuntimeError):
@@ -81,6 +82,13 @@ def load():
         lib.la_set_wait_limit.restype = None
         lib.la_set_column_split.argtypes = [ctypes.c_int]
         lib.la_set_column_split.restype = None
+        lib.la_extend_gqa.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, ip,
+                                      ip, vp, sz, vp]
+        lib.la_extend_gqa.restype = ip
+        lib.la_extend_gqa_workspace_size.argtypes = [ip, ip, ip, ip, ip, ip, ctypes.POINTER(sz)]
+        lib.la_extend_gqa_workspace_size.restype = ip
+        lib.la_decode_gqa.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, ip, vp]
+        lib.la_decode_gqa.restype = ip
         _lib = lib
         return lib
 
@@ -384,3 +392,74 @@ def commit_accepted(inter_states, accept_idx, state_pool, state_idx):
         st = load().la_commit_accepted(_ptr(inter_states), _ptr(accept_idx), _ptr(state_pool),
                                        num_slots, _ptr(state_idx), B, N, H, D, _stream_handle(dev))
     _check("la_commit_accepted", st)
+
+
+def extend_gqa_workspace_size(B: int, T: int, H: int, Hkv: int, D: int, max_seqlen: int) -> int:
+    """Bytes of scratch la_extend_gqa uses for this batch shape on the current device."""
+    n = ctypes.c_size_t(0)
+    _check("la_extend_gqa_workspace_size",
+           load().la_extend_gqa_workspace_size(B, T, H, Hkv, D, max_seqlen, ctypes.byref(n)))
+    return int(n.value)
+
+
+def extend_gqa(q, k, v, slopes_, state_pool, state_idx, cu_seqlens, prefix_mask, out=None,
+               max_seqlen: int | None = None, workspace=None):
+    """Grouped-query extend (la_extend_gqa): q bf16 [T, H*D]; k, v bf16 [T, Hkv*D]; slopes fp32
+    [Hkv]; state_pool fp32 [S, Hkv, D, D] updated in place; returns out bf16 [T, H*D].  H comes
+    from q, Hkv from the pool.  workspace: None lets the binding supply the scratch (a cached
+    per-device buffer); otherwise a uint8 CUDA tensor of at least extend_gqa_workspace_size()."""
+    dev = q.device
+    T = q.shape[0]
+    num_slots, Hkv, D, _ = state_pool.shape
+    H = q.shape[1] // D
+    B = state_idx.shape[0]
+    _need(q, "q", torch.bfloat16, dev, (T, H * D))
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (T, Hkv * D))
+    _need(slopes_, "slopes", torch.float32, dev, (Hkv,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, (B + 1,))
+    _need(prefix_mask, "prefix_mask", torch.uint8, dev, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (T, H * D))
+    if max_seqlen is None:
+        max_seqlen = T
+    with _on(dev):
+        if workspace is None:
+            nbytes = extend_gqa_workspace_size(B, T, H, Hkv, D, int(max_seqlen))
+            ws = _cached_workspace(dev, nbytes) if nbytes > 0 else None
+        else:
+            ws = workspace
+            _need(ws, "workspace", torch.uint8, dev)
+        st = load().la_extend_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                  num_slots, _ptr(state_idx), _ptr(cu_seqlens), _ptr(prefix_mask),
+                                  _ptr(out), B, T, H, Hkv, D, int(max_seqlen), _ptr(ws),
+                                  ws.numel() if ws is not None else 0, _stream_handle(dev))
+    _check("la_extend_gqa", st)
+    return out
+
+
+def decode_gqa(q, k, v, slopes_, state_pool, state_idx, out=None):
+    """Grouped-query decode (la_decode_gqa): q bf16 [B, H*D]; k, v bf16 [B, Hkv*D]; slopes fp32
+    [Hkv]; state_pool fp32 [S, Hkv, D, D] updated in place; returns out bf16 [B, H*D]."""
+    dev = q.device
+    num_slots, Hkv, D, _ = state_pool.shape
+    B = state_idx.shape[0]
+    H = q.shape[1] // D
+    _need(q, "q", torch.bfloat16, dev, (B, H * D))
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, dev, (B, Hkv * D))
+    _need(slopes_, "slopes", torch.float32, dev, (Hkv,))
+    _need(state_pool, "state_pool", torch.float32, dev)
+    _need(state_idx, "state_idx", torch.int32, dev, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev, (B, H * D))
+    with _on(dev):
+        st = load().la_decode_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes_), _ptr(state_pool),
+                                  num_slots, _ptr(state_idx), _ptr(out), B, H, Hkv, D,
+                                  _stream_handle(dev))
+    _check("la_decode_gqa", st)
+    return out

@@ -248,13 +248,39 @@ la_status la_commit_accepted(const float *inter_states, const int32_t *accept_id
 
 namespace {
 
+// Scratch of an extend call: the split plan's block states and initial-state copies, and for a
+// grouped call (Hkv < H) at least the initial-state copies.
+struct ExtendScratch {
+    la::SplitPlan plan;        // seg_len == 0: no sequence split
+    unsigned long long full;   // bytes with the split (0: no scratch at all)
+    unsigned long long copies; // bytes of the initial-state copies alone (grouped calls)
+};
+
+la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScratch *out) {
+    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull};
+    const unsigned long long mat = (unsigned long long)la::kHeadDim * la::kHeadDim * sizeof(float);
+    if (Hkv < H) out->copies = (unsigned long long)B * Hkv * mat;
+    out->full = out->copies;
+    if (B == 0 || T == 0) return LA_OK;
+    int sms = 0;
+    la_status st = num_sms(&sms);
+    if (st != LA_OK) return st;
+    const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead);
+    if (pl.seg_len > 0) {
+        out->plan = pl;
+        out->full = (unsigned long long)B * Hkv * (unsigned long long)(1 + pl.nblk) * mat;
+    }
+    return LA_OK;
+}
+
 la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
                       float *state_pool, int num_slots, const int32_t *state_idx,
                       const int32_t *cu_seqlens, const uint8_t *prefix_mask,
                       const int32_t *track_lens, const int32_t *track_state_idx, la_bf16 *out,
-                      long long out_rs, long long out_hs, int B, int T, int H, int D,
+                      long long out_rs, long long out_hs, int B, int T, int H, int Hkv, int D,
                       int max_seqlen, void *workspace, size_t workspace_bytes, la_stream stream) {
-    if (B < 0 || T < 0 || H < 1 || D < 1 || num_slots < 1 || max_seqlen < 0)
+    if (B < 0 || T < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || D < 1 || num_slots < 1 ||
+        max_seqlen < 0)
         return LA_ERR_INVALID;
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
     // output layout: 16-byte aligned rows and heads that do not overlap (rows of heads, or heads
@@ -271,6 +297,7 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     if (!slopes || !state_pool || !state_idx || !cu_seqlens || !prefix_mask) return LA_ERR_INVALID;
     if (T > 0 && (!q || !k || !v || !out)) return LA_ERR_INVALID;
     if ((long long)T * H * D >= (1ll << 40)) return LA_ERR_UNSUPPORTED;
+    if (workspace != nullptr && !aligned16(workspace)) return LA_ERR_INVALID;
     if (!aligned16(state_pool) || (T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
                                              !aligned16(out))))
         return LA_ERR_INVALID;
@@ -292,6 +319,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     p.B = B;
     p.T = T;
     p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
     p.num_slots = num_slots;
     p.max_seqlen = max_seqlen;
     const unsigned long long us = g_wait_limit.load();
@@ -306,17 +335,19 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     p.track_idx = track_state_idx;
     p.out_rs = out_rs;
     p.out_hs = out_hs;
-    if (workspace != nullptr && aligned16(workspace) && T > 0) {
-        int sms = 0;
-        if ((st = num_sms(&sms)) != LA_OK) return st;
-        const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead);
-        if (pl.seg_len > 0 && (unsigned long long)workspace_bytes >= pl.ws_bytes) {
-            p.seg_len = pl.seg_len;
-            p.blk_len = pl.blk_len;
-            p.nseg = pl.nseg;
-            p.nblk = pl.nblk;
-            p.ws = static_cast<float *>(workspace);
-        }
+    ExtendScratch scr;
+    if ((st = extend_scratch(B, T, H, Hkv, max_seqlen, &scr)) != LA_OK) return st;
+    // a grouped call cannot run without its initial-state copies
+    if (p.group > 1 && (workspace == nullptr || (unsigned long long)workspace_bytes < scr.copies))
+        return LA_ERR_INVALID;
+    if (p.group > 1) p.ws = static_cast<float *>(workspace);
+    if (workspace != nullptr && scr.plan.seg_len > 0 &&
+        (unsigned long long)workspace_bytes >= scr.full) {
+        p.seg_len = scr.plan.seg_len;
+        p.blk_len = scr.plan.blk_len;
+        p.nseg = scr.plan.nseg;
+        p.nblk = scr.plan.nblk;
+        p.ws = static_cast<float *>(workspace);
     }
     // Column split: SMs that one CTA per (request, head) leaves idle take the second value-column
     // half of the longest requests, H CTAs per request.
@@ -328,7 +359,7 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         if (spare >= H) p.csplit = (int)std::min<long long>(B, spare / H);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (p.seg_len > 0) {
+    if (p.seg_len > 0 || p.group > 1) {
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
@@ -345,8 +376,62 @@ la_status la_extend(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const 
                     int T, int H, int D, int max_seqlen, void *workspace, size_t workspace_bytes,
                     la_stream stream) {
     return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
-                       nullptr, nullptr, out, 0, 0, B, T, H, D, max_seqlen, workspace,
+                       nullptr, nullptr, out, 0, 0, B, T, H, H, D, max_seqlen, workspace,
                        workspace_bytes, stream);
+}
+
+la_status la_extend_gqa(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                        float *state_pool, int num_slots, const int32_t *state_idx,
+                        const int32_t *cu_seqlens, const uint8_t *prefix_mask, la_bf16 *out,
+                        int B, int T, int H, int Hkv, int D, int max_seqlen, void *workspace,
+                        size_t workspace_bytes, la_stream stream) {
+    return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
+                       nullptr, nullptr, out, 0, 0, B, T, H, Hkv, D, max_seqlen, workspace,
+                       workspace_bytes, stream);
+}
+
+la_status la_extend_gqa_workspace_size(int B, int T, int H, int Hkv, int D, int max_seqlen,
+                                       size_t *bytes) {
+    if (B < 0 || T < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || D < 1 || max_seqlen < 0 ||
+        bytes == nullptr)
+        return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    ExtendScratch scr;
+    const la_status st = extend_scratch(B, T, H, Hkv, max_seqlen, &scr);
+    if (st != LA_OK) return st;
+    *bytes = (size_t)scr.full;
+    return LA_OK;
+}
+
+la_status la_decode_gqa(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
+                        float *state_pool, int num_slots, const int32_t *state_idx, la_bf16 *out,
+                        int B, int H, int Hkv, int D, la_stream stream) {
+    if (B < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || D < 1 || num_slots < 1)
+        return LA_ERR_INVALID;
+    if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (Hkv == H)  // one query head per state: the plain decode
+        return la_decode(q, k, v, slopes, state_pool, num_slots, state_idx, out, B, H, D, stream);
+    if (B == 0) return LA_OK;
+    if (!q || !k || !v || !slopes || !state_pool || !state_idx || !out) return LA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_pool) ||
+        !aligned16(out) || !aligned4(slopes) || !aligned4(state_idx))
+        return LA_ERR_INVALID;
+    la::RecurParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.slopes = slopes;
+    p.pool = state_pool;
+    p.state_idx = state_idx;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.B = B;
+    p.H = Hkv;
+    p.G = H / Hkv;
+    p.N = 1;
+    p.num_slots = num_slots;
+    la_status st = error_word_ptr(&p.err);
+    if (st != LA_OK) return st;
+    return launch_status(la::launch_decode_grouped(p, static_cast<cudaStream_t>(stream)));
 }
 
 la_status la_extend_ex(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, const float *slopes,
@@ -358,7 +443,7 @@ la_status la_extend_ex(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, con
     if ((track_lens == nullptr) != (track_state_idx == nullptr)) return LA_ERR_INVALID;
     return extend_impl(q, k, v, slopes, state_pool, num_slots, state_idx, cu_seqlens, prefix_mask,
                        track_lens, track_state_idx, out, (long long)out_row_stride,
-                       (long long)out_head_stride, B, T, H, D, max_seqlen, workspace,
+                       (long long)out_head_stride, B, T, H, H, D, max_seqlen, workspace,
                        workspace_bytes, stream);
 }
 
@@ -366,12 +451,10 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
     if (B < 0 || T < 0 || H < 1 || D < 1 || max_seqlen < 0 || bytes == nullptr)
         return LA_ERR_INVALID;
     if (D != la::kHeadDim) return LA_ERR_UNSUPPORTED;
-    *bytes = 0;
-    if (B == 0 || T == 0) return LA_OK;
-    int sms = 0;
-    la_status st = num_sms(&sms);
+    ExtendScratch scr;
+    const la_status st = extend_scratch(B, T, H, H, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead).ws_bytes;
+    *bytes = (size_t)scr.full;
     return LA_OK;
 }
 

@@ -13,7 +13,9 @@
 //
 // The block-state kernel computes B_k for the blocks that precede a request's last segment, and
 // copies each split request's initial state S0 (its pool slot, or zero) into the workspace, so
-// that the extend kernel's segments never read a pool slot that the last segment rewrites.
+// that the extend kernel's segments never read a pool slot that the last segment rewrites.  For a
+// grouped-query call (several query heads per kv head) it copies every request's S0, for the same
+// reason: the group's first query head rewrites the slot that its siblings start from.
 //
 // One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
 // three stages); eight warps scale K by e^{-s (e - 1 - t)} into a bf16 pair hi (in place) + lo;
@@ -99,9 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int H = p.H;
-    const int k = blockIdx.x % p.nblk;
-    const int bh = blockIdx.x / p.nblk;
+    const int H = p.Hkv;  // the states' heads (kv heads of a grouped call)
+    const int nblk_grid = p.nblk > 0 ? p.nblk : 1;
+    const int k = blockIdx.x % nblk_grid;
+    const int bh = blockIdx.x / nblk_grid;
     const int h = bh % H;
     const int b = bh / H;
 
@@ -112,9 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kernel, launched next on the same stream, records these faults in the error word
     const int n = t1 - t0;
     if (n > p.max_seqlen) return;  // longer than the caller's bound: reported by the extend kernel
-    const int nseg_b = (n + p.seg_len - 1) / p.seg_len;
-    if (nseg_b <= 1) return;  // not split
-    const int per_seg = p.seg_len / p.blk_len;
+    const int nseg_b = p.seg_len > 0 ? (n + p.seg_len - 1) / p.seg_len : 1;
+    if (nseg_b <= 1 && p.group == 1) return;  // not split: nothing to copy or compute
     float *ws_bh = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) * (kHeadDim * kHeadDim);
 
     // The initial state S0 of a split request (pool slot if it has a prefix, else zero).
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<float4 *>(dst)[x] =
                 pre ? reinterpret_cast<const float4 *>(src)[x] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (nseg_b <= 1) return;  // grouped call, request not split: the copy was all
+    const int per_seg = p.seg_len / p.blk_len;
     if (k >= (nseg_b - 1) * per_seg) return;  // block at or after the last segment's start
 
     const int a = k * p.blk_len;               // block [a, e) relative to t0; always full length
@@ -316,11 +320,15 @@ SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_hea
 
 
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
-    const long long ctas = (long long)p.B * p.H * p.nblk;
-    if (p.seg_len <= 0 || ctas <= 0 || p.T <= 0) return cudaSuccess;
+    if (p.seg_len <= 0 && p.group == 1) return cudaSuccess;
+    const long long ctas = (long long)p.B * p.Hkv * (p.nblk > 0 ? p.nblk : 1);
+    if (ctas <= 0) return cudaSuccess;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap tk, tv;
-    if (!make_token_map_full(&tk, p.k, p.T, p.H) || !make_token_map_full(&tv, p.v, p.T, p.H))
+    memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv));
+    if (p.T > 0 && (!make_token_map_full(&tk, p.k, p.T, p.Hkv) ||
+                    !make_token_map_full(&tv, p.v, p.T, p.Hkv)))
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

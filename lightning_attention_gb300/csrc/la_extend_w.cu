@@ -294,6 +294,12 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int H = p.H;
+    // grouped-query heads: query head h reads kv head hk (k, v, slope, state); hk = h otherwise
+    const int Hkv = p.Hkv;
+    const int hk = p.group == 1 ? h : h / p.group;
+    // with a group, every query head's CTA carries the kv head's state and the group's first one
+    // writes it back
+    const bool writes_state = p.group == 1 || hk * p.group == h;
 
     // Request geometry, checked before anything is allocated (the exit is CTA-uniform).
     const int slot = p.state_idx[b];
@@ -386,7 +392,8 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int k_issued = 0, q_issued = 0, v_issued = 0, ys = 0;
-            const int xq = h * kHeadDim;
+            const int xq = h * kHeadDim;    // query head h in q
+            const int xkv = hk * kHeadDim;  // its kv head in k and v
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1;
                 const int y = t0 + (kEx ? ys : c * C);
@@ -398,8 +405,8 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
                     break;
                 uint8_t *kt = sm + OFF_K + st * SZ_T;
                 mbar_arrive_expect_tx(&bars->k_full[st], SZ_T);
-                tma_load_2d(kt, &tk, &bars->k_full[st], xq, y);
-                tma_load_2d(kt + 16384, &tk, &bars->k_full[st], xq + 64, y);
+                tma_load_2d(kt, &tk, &bars->k_full[st], xkv, y);
+                tma_load_2d(kt + 16384, &tk, &bars->k_full[st], xkv + 64, y);
                 k_issued = c + 1;
                 if (c >= 1 && !wait_bar(&bars->q_empty, (c - 1) & 1, limit, abort_flag, p.err))
                     break;
@@ -411,11 +418,11 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
                     break;
                 if constexpr (nv == kHeadDim) {
                     mbar_arrive_expect_tx(&bars->v_full, SZ_T);
-                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq, y);
-                    tma_load_2d(sm + OFF_V + 16384, &tv, &bars->v_full, xq + 64, y);
+                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xkv, y);
+                    tma_load_2d(sm + OFF_V + 16384, &tv, &bars->v_full, xkv + 64, y);
                 } else {
                     mbar_arrive_expect_tx(&bars->v_full, SZ_T / 2);
-                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xq + c0, y);
+                    tma_load_2d(sm + OFF_V, &tv, &bars->v_full, xkv + c0, y);
                 }
                 v_issued = c + 1;
             }
@@ -534,7 +541,7 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
         const int zb1 = cw == 1 ? 4 : q + 1;
         const int ku0 = kKUnits * warp;  // units ku0 .. ku0 + kKUnits - 1
 
-        const float slope = p.slopes[h];
+        const float slope = p.slopes[hk];
         for (int m = threadIdx.x; m <= C; m += kEpiThreads) {
             const float e = expf(-slope * (float)m);
             tab[m] = e;
@@ -546,7 +553,7 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
         uint8_t *s_hi = sm + OFF_SHI;
         uint8_t *s_lo = sm + OFF_SLO;
         // this row's share of the pool state: value columns c0 + col_base .. + 32 nsubs - 1
-        float *gstate = p.pool + (((size_t)slot * H + h) * kHeadDim + i) * kHeadDim +
+        float *gstate = p.pool + (((size_t)slot * Hkv + hk) * kHeadDim + i) * kHeadDim +
                         (size_t)(c0 + col_base);
         {
             const int r0 = nchunks > 0 ? chunk_len(kEx, 0, sp, n) : 0;
@@ -555,10 +562,11 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
             for (int sub = 0; sub < nsubs; ++sub) {
                 const int col0 = col_base + sub * 32;
                 float S[32];
-                if (split) {
+                if (split || p.group > 1) {
                     // S = e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, from
-                    // the workspace the block-state kernel filled.
-                    const float *w0 = p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) *
+                    // the workspace the block-state kernel filled (the S0 copy alone for an
+                    // unsplit request of a grouped call).
+                    const float *w0 = p.ws + ((size_t)b * Hkv + hk) * (size_t)(1 + p.nblk) *
                                                  (kHeadDim * kHeadDim) +
                                       (size_t)i * kHeadDim + c0 + col0;
                     const float d0 = expf(-slope * (float)g * (float)p.seg_len);
@@ -570,7 +578,7 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
                         S[4 * x + 2] = d0 * f.z;
                         S[4 * x + 3] = d0 * f.w;
                     }
-                    const int nb = g * (p.seg_len / p.blk_len);
+                    const int nb = split ? g * (p.seg_len / p.blk_len) : 0;
                     for (int kb = 0; kb < nb; ++kb) {
                         const float dk =
                             expf(-slope * (float)(g * p.seg_len - (kb + 1) * p.blk_len));
@@ -811,7 +819,7 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
         }
         // Final state write-back (also for zero-length requests).  Skipped after an abort: the
         // error word already reports the failure.  The last state pass left S unscaled.
-        if (ok && !*abort_flag && last_seg) {
+        if (ok && !*abort_flag && last_seg && writes_state) {
 #pragma unroll 1
             for (int sub = 0; sub < nsubs; ++sub) {
                 uint32_t w[32];
@@ -941,8 +949,9 @@ cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream) {
     memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv));
     if (p.T > 0) {
-        if (!make_token_map_full(&tq, p.q, p.T, p.H) || !make_token_map_full(&tk, p.k, p.T, p.H) ||
-            !make_token_map_full(&tv, p.v, p.T, p.H))
+        if (!make_token_map_full(&tq, p.q, p.T, p.H) ||
+            !make_token_map_full(&tk, p.k, p.T, p.Hkv) ||
+            !make_token_map_full(&tv, p.v, p.T, p.Hkv))
             return cudaErrorInvalidValue;
     }
     int dev = 0;

@@ -32,10 +32,15 @@ struct RecurParams {
     const int32_t *parents;      // [B][N] (tree verify)
     __nv_bfloat16 *out;
     unsigned int *err;           // device error word
-    int B, H, N, num_slots;
+    int B, H, N, num_slots;      // H: heads of k, v, slopes and the states
+    int G;                       // query heads per state (grouped decode; 1 otherwise): q and out
+                                 // have H * G heads, query head h reads state h / G
 };
 
 cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream);
+// Grouped-query decode: one CTA per (request, kv head) advances the state once and reads it out
+// for each of its p.G query heads.
+cudaError_t launch_decode_grouped(const RecurParams &p, cudaStream_t stream);
 
 // Accepted-state commit: pool[state_idx[b]] = inter[b][accept_idx[b]] (all heads) when
 // accept_idx[b] >= 0.
@@ -60,6 +65,12 @@ struct ExtendParams {
     __nv_bfloat16 *out;
     unsigned int *err;
     int B, T, H, num_slots, max_seqlen;
+    // Grouped-query heads: q and out have H heads; k, v, slopes, the pool and the workspace have
+    // Hkv = H / group heads, and query head h reads kv head h / group (group 1: plain).  With
+    // group > 1 every query head's CTA carries its kv head's state; the first query head of the
+    // group writes the final state, and all of them start from the workspace copy of the
+    // initial state (written by the block-state kernel), so that write races no read.
+    int Hkv, group;
     unsigned long long wait_limit_ns;  // bound on every mbarrier wait
     // Sequence split of long requests (seg_len == 0: none).  A request of n tokens is cut into
     // segments of seg_len tokens, processed by separate CTAs; segment g starts from
@@ -70,7 +81,7 @@ struct ExtendParams {
     int blk_len;   // multiple of the chunk length
     int nseg;      // segments per request, upper bound over the batch
     int nblk;      // blocks per request kept in the workspace
-    float *ws;     // [B][H][1 + nblk][D][D]: S0 copy, then block states
+    float *ws;     // [B][Hkv][1 + nblk][D][D]: S0 copy, then block states
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
     // Column split (0: none; only without a sequence split).  The csplit longest requests run as
     // two CTAs per head, one per 64-column half of the values, which shortens their chunk chains
@@ -99,6 +110,8 @@ cudaError_t launch_extend_wide(const ExtendParams &p, cudaStream_t stream);  // 
 // [T][H*128] bf16 TMA map, box of 64 columns x 128 rows, 128-byte swizzle; rows past T read as
 // zero (la_extend_w.cu).
 bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);
+// The pre-pass of a split or grouped extend: the workspace copy of each initial state, and the
+// block states of split requests (la_extend_seg.cu).  Launched when p.seg_len > 0 or p.group > 1.
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
 
 }  // namespace la

@@ -164,6 +164,88 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
     }
 }
 
+// Grouped-query decode: CTA (b, j) advances the state of kv head j of request b by one token and
+// reads it out for the G query heads j G .. j G + G - 1, so each state crosses HBM once however
+// many query heads share it.  Thread layout, vector widths and the per-token arithmetic are those
+// of recurrent_kernel; the readouts meet in the same double-buffered shared memory, one barrier
+// per query head.
+__global__ void __launch_bounds__(kThreads) decode_grouped_kernel(const RecurParams p) {
+    const int H = p.H;  // kv heads
+    const int G = p.G;
+    const int b = blockIdx.x / H;
+    const int j = blockIdx.x - b * H;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row0 = warp * kRowsPerWarp;
+    const int col = lane * 4;
+
+    __shared__ __align__(16) float red[2][kWarps][kHeadDim];
+
+    const int slot = p.state_idx[b];
+    if (slot < 0 || slot >= p.num_slots) {
+        if (threadIdx.x == 0) atomicOr(p.err, ERR_BIT_SLOT_RANGE);
+        return;
+    }
+    float *state = p.pool + ((size_t)slot * H + j) * (size_t)(kHeadDim * kHeadDim);
+    float4 s[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+        s[r] = __ldcs(reinterpret_cast<const float4 *>(state + (size_t)(row0 + r) * kHeadDim + col));
+
+    const float decay = expf(-p.slopes[j]);
+    const size_t kv = (size_t)b * H * kHeadDim + (size_t)j * kHeadDim;
+    const uint4 *kp = reinterpret_cast<const uint4 *>(p.k + kv + row0);
+    const uint2 vv = *reinterpret_cast<const uint2 *>(p.v + kv + col);
+    float kf[16];
+    unpack8(kp[0], kf);
+    unpack8(kp[1], kf + 8);
+    const float v0 = bf_lo(vv.x), v1 = bf_hi(vv.x), v2 = bf_lo(vv.y), v3 = bf_hi(vv.y);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        // S = S * exp(-slope_j) + outer(k, v), once for the whole group
+        s[r].x = fmaf(kf[r], v0, s[r].x * decay);
+        s[r].y = fmaf(kf[r], v1, s[r].y * decay);
+        s[r].z = fmaf(kf[r], v2, s[r].z * decay);
+        s[r].w = fmaf(kf[r], v3, s[r].w * decay);
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+        __stcs(reinterpret_cast<float4 *>(state + (size_t)(row0 + r) * kHeadDim + col), s[r]);
+
+    const size_t q_row = (size_t)H * G * kHeadDim;
+    for (int g = 0; g < G; ++g) {
+        const size_t qo = (size_t)b * q_row + (size_t)(j * G + g) * kHeadDim;
+        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + qo + row0);
+        float qf[16];
+        unpack8(qp[0], qf);
+        unpack8(qp[1], qf + 8);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            o.x = fmaf(qf[r], s[r].x, o.x);
+            o.y = fmaf(qf[r], s[r].y, o.y);
+            o.z = fmaf(qf[r], s[r].z, o.z);
+            o.w = fmaf(qf[r], s[r].w, o.w);
+        }
+        float(*buf)[kHeadDim] = red[g & 1];
+        *reinterpret_cast<float4 *>(&buf[warp][col]) = o;
+        __syncthreads();
+        if (threadIdx.x < kHeadDim / 2) {
+            const int jj = threadIdx.x * 2;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                a0 += buf[w][jj];
+                a1 += buf[w][jj + 1];
+            }
+            *reinterpret_cast<__nv_bfloat162 *>(p.out + qo + jj) =
+                __floats2bfloat162_rn(a0 * kScale, a1 * kScale);
+        }
+        // red[g & 1] is rewritten at query head g + 2, after every reader of head g has passed
+        // the barrier of head g + 1
+    }
+}
+
 // One CTA of 256 threads per (request, head): a 64 KiB fp32 copy with 16-byte accesses.
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitParams p) {
     const int b = blockIdx.x / p.H;
@@ -198,6 +280,14 @@ cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream) {
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     commit_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_grouped(const RecurParams &p, cudaStream_t stream) {
+    const long long blocks = (long long)p.B * p.H;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_grouped_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

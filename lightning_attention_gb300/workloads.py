@@ -50,6 +50,8 @@ class Workload:
     track_lens: torch.Tensor | None = None   # int32 [B] (extend with state tracking)
     track_idx: torch.Tensor | None = None    # int32 [B] (extend with state tracking)
     accept_idx: torch.Tensor | None = None   # int32 [B] (verify followed by the commit)
+    Hkv: int | None = None                   # kv heads of a grouped-query workload (None: H);
+                                             # k, v, slopes and the pool then have Hkv heads
 
     @property
     def B(self) -> int:
@@ -62,12 +64,17 @@ class Workload:
     def tokens(self) -> int:
         return self.T
 
+    @property
+    def state_heads(self) -> int:
+        """Heads of k, v, the slopes and the states (the kv heads of a grouped workload)."""
+        return self.H if self.Hkv is None else self.Hkv
+
     def materialize_pool(self, device="cpu") -> torch.Tensor:
         """Full fp32 pool [num_slots, H, D, D] on ``device``: sentinel everywhere, prefix states
         in the slots of prefix requests, NaN in the named slots of the other requests."""
         if self.random_pool:
             return self.pool_fill.to(device).clone()
-        pool = torch.full((self.num_slots, self.H, self.D, self.D), SENTINEL,
+        pool = torch.full((self.num_slots, self.state_heads, self.D, self.D), SENTINEL,
                           dtype=torch.float32, device=device)
         for b in range(self.B):
             s = int(self.state_idx[b])
@@ -249,6 +256,50 @@ def custom_verify(B: int, N: int, H: int = 2, D: int = HEAD_DIM, layer_id: int =
     return Workload(name=f"custom_verify_{B}x{N}", kind="verify", H=H, D=D, layer_id=layer_id,
                     L=L, num_slots=ns, q=q, k=k, v=v, state_idx=idx,
                     prefix_mask=torch.ones(B, dtype=torch.uint8), prefix_states=ps, N=N)
+
+
+def custom_extend_gqa(lengths, H: int, Hkv: int, D: int = HEAD_DIM, layer_id: int = 0, L: int = 1,
+                      prefix=None, num_slots: int | None = None, seed: int = 0) -> Workload:
+    """Grouped-query extend batch: q with H heads, k and v with Hkv heads (H a multiple of Hkv),
+    prefix states per kv head.  Draw order: q, k, v, prefix states, slot permutation."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(lengths)
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    if B:
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    T = int(cu[-1])
+    q = torch.randn(T, H * D, generator=g).to(torch.bfloat16)
+    k = torch.randn(T, Hkv * D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv * D, generator=g).to(torch.bfloat16)
+    if prefix is None:
+        prefix = [b % 2 for b in range(B)]
+    pm = torch.tensor(list(prefix), dtype=torch.uint8) if B else torch.zeros(0, dtype=torch.uint8)
+    ps = torch.zeros(B, Hkv, D, D)
+    for b in range(B):
+        if pm[b]:
+            ps[b] = torch.randn(Hkv, D, D, generator=g) * 0.05
+    ns = num_slots if num_slots is not None else max(2 * B, 1)
+    idx = torch.randperm(ns, generator=g)[:B].to(torch.int32)
+    return Workload(name=f"custom_gqa_{B}req_h{H}_kv{Hkv}", kind="extend", H=H, D=D,
+                    layer_id=layer_id, L=L, num_slots=ns, q=q, k=k, v=v, state_idx=idx,
+                    prefix_mask=pm, prefix_states=ps, cu_seqlens=cu, Hkv=Hkv)
+
+
+def custom_decode_gqa(B: int, H: int, Hkv: int, D: int = HEAD_DIM, layer_id: int = 0, L: int = 1,
+                      num_slots: int | None = None, seed: int = 0) -> Workload:
+    """Grouped-query decode batch: q [B, H*D], k and v [B, Hkv*D], a random pool of Hkv-head
+    states (N(0,1)*0.05) with the B slots a random permutation subset."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H * D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv * D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv * D, generator=g).to(torch.bfloat16)
+    ns = num_slots if num_slots is not None else 2 * B
+    pool = torch.randn(ns, Hkv, D, D, generator=g) * 0.05
+    idx = torch.randperm(ns, generator=g)[:B].to(torch.int32)
+    return Workload(name=f"custom_decode_gqa_b{B}_h{H}_kv{Hkv}", kind="decode", H=H, D=D,
+                    layer_id=layer_id, L=L, num_slots=ns, q=q, k=k, v=v, state_idx=idx,
+                    prefix_mask=torch.ones(B, dtype=torch.uint8), prefix_states=torch.empty(0),
+                    random_pool=True, pool_fill=pool, Hkv=Hkv)
 
 
 WORKLOADS = {
