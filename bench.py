@@ -13,6 +13,8 @@ A step is one call of the path over one batch of the chosen workload (inputs res
   verify_tree    the same requests with an 8-token binary draft tree each
   varlen_extend_tracked  varlen_extend plus a state-tracking snapshot per request
   verify_commit  verify followed by the accepted-state commit (two library calls)
+  varlen_extend_b1024  1024 requests, lengths uniform in [32, 512], H=16 (longest first through
+                 the ranking pre-pass; also timed in index order)
 Every workload's inputs exceed the 129 MB L2, so no flush is needed between steps.  With N > 1
 (torchrun), every rank runs its own replica of the workload (weak scaling, no collective on the
 data path); timing is bracketed by a barrier and the slowest rank's time is reported.
@@ -63,6 +65,7 @@ KERNEL_SOURCE = {
     "verify_tree": "la_recurrent.cu",
     "varlen_extend_tracked": "la_extend_w.cu",
     "verify_commit": "la_recurrent.cu",
+    "varlen_extend_b1024": ("la_extend_w.cu", "la_extend_seg.cu"),
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
@@ -72,6 +75,7 @@ KERNEL_NAME = {
     "verify_tree": "recurrent_kernel<3>",
     "varlen_extend_tracked": "extend_wide_kernel",
     "verify_commit": "recurrent_kernel<1>",
+    "varlen_extend_b1024": "extend_wide_kernel",
 }
 # Small cases of the same kernels for multi-pass ncu captures (--profile-calls); a few GB at most.
 PROFILE_CASES = {
@@ -299,10 +303,16 @@ class GpuCase:
             self.pm = w.prefix_mask.to(dev)
             lens = w.cu_seqlens[1:] - w.cu_seqlens[:-1]
             self.max_seqlen = int(lens.max()) if w.B else 0
+            self.workspace = None  # the binding supplies what la_extend_workspace_size asks for
             if la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen) > 0:
-                # long requests split into segments: block-state kernel, then the extend kernel
-                self.launches_per_step = 2
-                self.kernel = "block_state_kernel + extend_wide_kernel (one la_extend call)"
+                if w.B > 256:
+                    # a large batch: the ranking pre-pass, then the extend kernel
+                    self.launches_per_step = 2
+                    self.kernel = "rank_requests_kernel + extend_wide_kernel (one la_extend call)"
+                else:
+                    # long requests split into segments: block-state kernel, then the extend kernel
+                    self.launches_per_step = 2
+                    self.kernel = "block_state_kernel + extend_wide_kernel (one la_extend call)"
             self.track = None
             if w.track_lens is not None:
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
@@ -341,7 +351,7 @@ class GpuCase:
                       track_state_idx=self.track[1])
         else:
             la.extend(q, k, v, self.slopes, self.pool, idx, self.cu, self.pm, out=out,
-                      max_seqlen=self.max_seqlen)
+                      max_seqlen=self.max_seqlen, workspace=self.workspace)
         return out
 
 
@@ -418,6 +428,18 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
                                  "the state update and P V each as a bf16 hi + lo pair; the "
                                  "time includes every launch of the call"}
 
+    index_order = None
+    if w.kind == "extend" and w.B > 256 and w.track_lens is None:
+        # the same batch in index order (no workspace: no ranking pre-pass), for comparison
+        case.workspace = False
+        case.launches_per_step -= 1
+        case.step()
+        io_s, _ = timed_region(case, steps, world, dev, stream)
+        case.workspace = None
+        case.launches_per_step += 1
+        index_order = {"ms_per_step": round(max_over_ranks(io_s, world, dev) / steps * 1e3, 4),
+                       "note": "requests in index order instead of longest first"}
+
     e2e = None
     if with_e2e:
         e2e = time_e2e(case, w, geo, steps, world, dev)
@@ -425,7 +447,7 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
            "gpu_launches": steps * case.launches_per_step,
            "host_enqueue_us_per_call": round(host_s / steps * 1e6, 2),
            "roofline": roof, "wall_s": wall1 - wall0, "clocks": clocks, "e2e": e2e,
-           "workload": w, "geo": geo, "spread": spread}
+           "workload": w, "geo": geo, "spread": spread, "index_order": index_order}
     if tensor:
         res["tensor"] = tensor
     return res
@@ -589,7 +611,8 @@ def run_oracle_sample(w, sample, threads):
 
 ORACLE_BUDGET = {  # (request, head) pairs or token-heads per sample: ~1-10 s of fp64 CPU work
     "decode": 4096, "verify": 64 * 5 * 16, "varlen_extend": 16 * 2400, "long_prefill": 32 * 1200,
-    "verify_tree": 64 * 8 * 8, "varlen_extend_tracked": 16 * 2400, "verify_commit": 64 * 5 * 16}
+    "verify_tree": 64 * 8 * 8, "varlen_extend_tracked": 16 * 2400, "verify_commit": 64 * 5 * 16,
+    "varlen_extend_b1024": 16 * 2400}
 
 
 def cpu_baseline(name, w, threads):
@@ -676,6 +699,8 @@ def main():
             "clocks": head["clocks"]}
     if "tensor" in head:
         line["tensor"] = head["tensor"]
+    if head.get("index_order"):
+        line["index_order"] = head["index_order"]
     threads = os.cpu_count() or 1
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args.workload, w, threads)
@@ -706,8 +731,8 @@ def main():
 # The other workloads, each timed like the headline (3 repeats of up to 20 steps, clocks sampled
 # over them).  The chain verify of 128 x 5 draft tokens comes last so that it is in the tail of
 # the printed line.
-OTHER_ORDER = ("verify_tree", "varlen_extend_tracked", "verify_commit", "varlen_extend",
-               "long_prefill", "verify")
+OTHER_ORDER = ("varlen_extend_b1024", "verify_tree", "varlen_extend_tracked", "verify_commit",
+               "varlen_extend", "long_prefill", "verify")
 
 
 def compact_entry(r, steps, cpu):
@@ -720,6 +745,8 @@ def compact_entry(r, steps, cpu):
                       "kernel": roof["kernel"]},
          "gpu_launches": r["gpu_launches"],
          "host_enqueue_us_per_call": r["host_enqueue_us_per_call"]}
+    if r.get("index_order"):
+        e["index_order"] = r["index_order"]
     if r.get("clocks"):
         c = r["clocks"]
         e["clocks"] = {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),

@@ -252,16 +252,24 @@ namespace {
 // grouped call (Hkv < H) at least the initial-state copies.
 struct ExtendScratch {
     la::SplitPlan plan;        // seg_len == 0: no sequence split
-    unsigned long long full;   // bytes with the split (0: no scratch at all)
+    unsigned long long full;   // bytes with the split, before the order array
     unsigned long long copies; // bytes of the initial-state copies alone (grouped calls)
+    unsigned long long order;  // bytes of the longest-first order array (large batches), after
+                               // `full`
 };
 
+// Up to this many requests every extend CTA ranks the batch itself; above it, a pre-pass ranks
+// it once into the workspace.
+constexpr int kInCtaRankedRequests = 256;
+
 la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScratch *out) {
-    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull};
+    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull, 0ull};
     const unsigned long long mat = (unsigned long long)la::kHeadDim * la::kHeadDim * sizeof(float);
     if (Hkv < H) out->copies = (unsigned long long)B * Hkv * mat;
     out->full = out->copies;
     if (B == 0 || T == 0) return LA_OK;
+    if (B > kInCtaRankedRequests && B <= la::kMaxRankedRequests)
+        out->order = ((unsigned long long)B * sizeof(int32_t) + 15ull) & ~15ull;
     int sms = 0;
     la_status st = num_sms(&sms);
     if (st != LA_OK) return st;
@@ -330,7 +338,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     p.nseg = 1;
     p.nblk = 0;
     p.ws = nullptr;
-    p.lpt = (B > 1 && B <= 256) ? 1 : 0;
+    p.lpt = (B > 1 && B <= kInCtaRankedRequests) ? 1 : 0;
+    p.order = nullptr;
     p.track_lens = track_lens;
     p.track_idx = track_state_idx;
     p.out_rs = out_rs;
@@ -349,6 +358,14 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         p.nblk = scr.plan.nblk;
         p.ws = static_cast<float *>(workspace);
     }
+    // a large batch is taken longest first when the workspace has room for its order
+    int32_t *order = nullptr;
+    if (workspace != nullptr && scr.order > 0 &&
+        (unsigned long long)workspace_bytes >= scr.full + scr.order) {
+        order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + scr.full);
+        p.order = order;
+        p.lpt = 1;
+    }
     // Column split: SMs that one CTA per (request, head) leaves idle take the second value-column
     // half of the longest requests, H CTAs per request.
     p.csplit = 0;
@@ -359,6 +376,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         if (spare >= H) p.csplit = (int)std::min<long long>(B, spare / H);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (order != nullptr && la::launch_rank_requests(cu_seqlens, B, order, s) != cudaSuccess)
+        return LA_ERR_CUDA;
     if (p.seg_len > 0 || p.group > 1) {
         const cudaError_t e = la::launch_block_states(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
@@ -399,7 +418,7 @@ la_status la_extend_gqa_workspace_size(int B, int T, int H, int Hkv, int D, int 
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, Hkv, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)scr.full;
+    *bytes = (size_t)(scr.full + scr.order);
     return LA_OK;
 }
 
@@ -454,7 +473,7 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, H, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)scr.full;
+    *bytes = (size_t)(scr.full + scr.order);
     return LA_OK;
 }
 

@@ -319,6 +319,41 @@ SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_hea
 }
 
 
+namespace {
+
+// order[rank of b] = b, the rank of request b being the number of requests that are longer, or
+// as long with a smaller index: a strict total order, so the ranks are a permutation even for
+// inconsistent cu_seqlens (which the extend kernel reports).  The lengths are staged through
+// shared memory 256 at a time.
+__global__ void __launch_bounds__(256) rank_requests_kernel(const int32_t *cu_seqlens, int B,
+                                                            int32_t *order) {
+    __shared__ int lens[256];
+    const int b = blockIdx.x * 256 + threadIdx.x;
+    const int lb = b < B ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+    int rank = 0;
+    for (int u0 = 0; u0 < B; u0 += 256) {
+        __syncthreads();
+        const int u = u0 + threadIdx.x;
+        lens[threadIdx.x] = u < B ? cu_seqlens[u + 1] - cu_seqlens[u] : 0;
+        __syncthreads();
+        const int m = min(256, B - u0);
+        for (int x = 0; x < m; ++x) {
+            const int lu = lens[x];
+            rank += (lu > lb) || (lu == lb && u0 + x < b);
+        }
+    }
+    if (b < B) order[rank] = b;
+}
+
+}  // namespace
+
+cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *order,
+                                 cudaStream_t stream) {
+    if (B <= 0) return cudaSuccess;
+    rank_requests_kernel<<<(unsigned)((B + 255) / 256), 256, 0, stream>>>(cu_seqlens, B, order);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
     if (p.seg_len <= 0 && p.group == 1) return cudaSuccess;
     const long long ctas = (long long)p.B * p.Hkv * (p.nblk > 0 ? p.nblk : 1);

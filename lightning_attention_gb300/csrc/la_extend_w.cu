@@ -876,7 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     int b = want;
-    if (p.lpt) {
+    if (p.lpt && p.order != nullptr) {
+        b = p.order[want];  // ranked by the pre-pass
+    } else if (p.lpt) {
         // Longest request first: CTAs are issued in index order, so taking requests in
         // decreasing length order (ties by index) keeps long requests from finishing last.
         __shared__ int s_req;

@@ -83,6 +83,10 @@ struct ExtendParams {
     int nblk;      // blocks per request kept in the workspace
     float *ws;     // [B][Hkv][1 + nblk][D][D]: S0 copy, then block states
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
+    // With lpt: the requests in decreasing length order (ties by index), written by the ranking
+    // pre-pass into the workspace for large batches; null: every CTA ranks the (few) requests
+    // itself.
+    const int32_t *order;
     // Column split (0: none; only without a sequence split).  The csplit longest requests run as
     // two CTAs per head, one per 64-column half of the values, which shortens their chunk chains
     // when the batch leaves SMs idle; the grid has (B + csplit) H CTAs.
@@ -113,5 +117,11 @@ bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);
 // The pre-pass of a split or grouped extend: the workspace copy of each initial state, and the
 // block states of split requests (la_extend_seg.cu).  Launched when p.seg_len > 0 or p.group > 1.
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
+// Longest-first order of a batch's requests: order[rank] = request, ranks by decreasing length,
+// ties by index (la_extend_seg.cu).  One thread per request compares it with every other.
+cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *order,
+                                 cudaStream_t stream);
+// Batches above this size keep index order (the ranking's work grows as B^2).
+constexpr int kMaxRankedRequests = 65536;
 
 }  // namespace la

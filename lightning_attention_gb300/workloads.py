@@ -148,6 +148,16 @@ def varlen_extend(seed: int = 0, B: int = 8, lo: int = 512, hi: int = 4096,
                     prefix_states=prefix, cu_seqlens=cu)
 
 
+def varlen_extend_many(seed: int = 0, B: int = 1024, lo: int = 32, hi: int = 512,
+                       num_slots: int = 2048) -> Workload:
+    """Large varlen extend batch: 1024 requests with lengths uniform in [32, 512], H=16, layer 0
+    of L=4; the even-indexed half carry prefix states; slots shuffled in a 2048-slot pool.  The
+    same draw order as varlen_extend."""
+    w = varlen_extend(seed, B=B, lo=lo, hi=hi, num_slots=num_slots)
+    w.name = f"varlen_extend_b{B}_h16"
+    return w
+
+
 def long_prefill(seed: int = 0, T: int = 32768, H: int = 32) -> Workload:
     """Long single-sequence prefill: one request of 32768 tokens, H=32, layer 5 of L=12, zero
     initial state; pool of 4 slots, the request in slot 1."""
@@ -311,4 +321,5 @@ WORKLOADS = {
     "verify_tree": verify_tree,
     "varlen_extend_tracked": varlen_extend_tracked,
     "verify_commit": verify_commit,
+    "varlen_extend_b1024": varlen_extend_many,
 }

@@ -188,3 +188,30 @@ def test_verify_small_and_decode_identity():
         assert torch.equal(o.cpu(), out.cpu()[rows])
         idx = w.state_idx.long()
         assert torch.equal(pool2.cpu()[idx], inter.cpu()[:, t])
+
+
+def test_large_batch_longest_first_changes_only_the_schedule():
+    """Above 256 requests the longest-first order comes from a ranking pre-pass into the
+    workspace.  Every (request, head) is computed the same way in any order, so the result equals
+    the index-order run (no workspace) bit for bit, and the oracle within the tolerance.  Many
+    equal lengths exercise the ties (broken by request index)."""
+    rng = np.random.default_rng(17)
+    lengths = [int(x) for x in rng.choice([0, 1, 37, 128, 129, 200, 300], size=600)]
+    w = workloads.custom_extend(lengths, H=2, layer_id=1, L=3, seed=19)
+    assert la.extend_workspace_size(w.B, w.T, w.H, 128, 300) >= 4 * w.B
+    args = (w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), la.slopes(2, 1, 3).to(DEV))
+    rest = (w.state_idx.to(DEV), w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV))
+    pool_a, pool_b = w.materialize_pool(DEV), w.materialize_pool(DEV)
+    out_a = la.extend(*args, pool_a, *rest, max_seqlen=300)                   # ranked
+    out_b = la.extend(*args, pool_b, *rest, max_seqlen=300, workspace=False)  # index order
+    la.poll_error()
+    assert torch.equal(out_a.cpu(), out_b.cpu())
+    assert torch.equal(pool_a.cpu().view(torch.int32), pool_b.cpu().view(torch.int32))
+    pool0 = w.materialize_pool()
+    o_ref, p_ref = oracle.extend(w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy(),
+                                 oracle_slopes_fp32(2, 1, 3), pool0.double().numpy(),
+                                 w.state_idx.numpy(), w.cu_seqlens.numpy(), w.prefix_mask.numpy(),
+                                 2, 128)
+    assert_close(to64(out_a), o_ref, "large batch: out")
+    idx = w.state_idx.numpy()
+    assert_close(pool_a.cpu().double().numpy()[idx], p_ref[idx], "large batch: states")
