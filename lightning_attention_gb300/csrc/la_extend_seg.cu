@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (base - raw);
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+    pdl_wait();
+    pdl_trigger();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -327,6 +329,8 @@ namespace {
 // shared memory 256 at a time.
 __global__ void __launch_bounds__(256) rank_requests_kernel(const int32_t *cu_seqlens, int B,
                                                             int32_t *order) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int lens[256];
     const int b = blockIdx.x * 256 + threadIdx.x;
     const int lb = b < B ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
@@ -350,8 +354,8 @@ __global__ void __launch_bounds__(256) rank_requests_kernel(const int32_t *cu_se
 cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *order,
                                  cudaStream_t stream) {
     if (B <= 0) return cudaSuccess;
-    rank_requests_kernel<<<(unsigned)((B + 255) / 256), 256, 0, stream>>>(cu_seqlens, B, order);
-    return cudaGetLastError();
+    return launch_pdl(rank_requests_kernel, dim3((unsigned)((B + 255) / 256)), dim3(256), 0, stream,
+                      cu_seqlens, B, order);
 }
 
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
@@ -380,8 +384,8 @@ cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {
             configured[dev] = true;
         }
     }
-    block_state_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(block_state_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes, stream,
+                      tk, tv, p);
 }
 
 }  // namespace la

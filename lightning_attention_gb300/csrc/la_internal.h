@@ -6,7 +6,37 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace la {
+
+// Programmatic dependent launch.  Every kernel of the library is launched with programmatic
+// stream serialization, so that it may be scheduled while the previous kernel on the stream
+// drains; it calls pdl_wait() before its first global-memory access (which returns once that
+// kernel has completed and its writes are visible, at once when there is none in flight) and
+// pdl_trigger() right after, so that the next kernel may be scheduled in turn.  A predecessor
+// that never triggers (any kernel outside the library) is simply waited for, as without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Bits of the per-device error word (see la_api.cu).
 enum : unsigned int {

@@ -39,6 +39,8 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int H = p.H;
     const int b = blockIdx.x / H;
     const int h = blockIdx.x - b * H;
@@ -170,6 +172,8 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurParams p
 // of recurrent_kernel; the readouts meet in the same double-buffered shared memory, one barrier
 // per query head.
 __global__ void __launch_bounds__(kThreads) decode_grouped_kernel(const RecurParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int H = p.H;  // kv heads
     const int G = p.G;
     const int b = blockIdx.x / H;
@@ -248,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) decode_grouped_kernel(const RecurPar
 
 // One CTA of 256 threads per (request, head): a 64 KiB fp32 copy with 16-byte accesses.
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x / p.H;
     const int h = blockIdx.x - b * p.H;
     const int slot = p.state_idx[b];
@@ -279,16 +285,14 @@ cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    commit_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(commit_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
 }
 
 cudaError_t launch_decode_grouped(const RecurParams &p, cudaStream_t stream) {
     const long long blocks = (long long)p.B * p.H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    decode_grouped_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_grouped_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, p);
 }
 
 cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t stream) {
@@ -297,11 +301,14 @@ cudaError_t launch_recurrent(RecurMode mode, const RecurParams &p, cudaStream_t 
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks), block(kThreads);
     switch (mode) {
-        case RECUR_DECODE: recurrent_kernel<RECUR_DECODE><<<grid, block, 0, stream>>>(p); break;
-        case RECUR_VERIFY: recurrent_kernel<RECUR_VERIFY><<<grid, block, 0, stream>>>(p); break;
-        case RECUR_TREE: recurrent_kernel<RECUR_TREE><<<grid, block, 0, stream>>>(p); break;
+        case RECUR_DECODE:
+            return launch_pdl(recurrent_kernel<RECUR_DECODE>, grid, block, 0, stream, p);
+        case RECUR_VERIFY:
+            return launch_pdl(recurrent_kernel<RECUR_VERIFY>, grid, block, 0, stream, p);
+        case RECUR_TREE:
+            return launch_pdl(recurrent_kernel<RECUR_TREE>, grid, block, 0, stream, p);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace la
