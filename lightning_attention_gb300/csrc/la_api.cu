@@ -379,7 +379,8 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     if (order != nullptr && la::launch_rank_requests(cu_seqlens, B, order, s) != cudaSuccess)
         return LA_ERR_CUDA;
     if (p.seg_len > 0 || p.group > 1) {
-        const cudaError_t e = la::launch_block_states(p, s);
+        cudaError_t e = la::launch_block_states(p, s);
+        if (e == cudaSuccess) e = la::launch_state_scan(p, s);
         if (e != cudaSuccess) return LA_ERR_CUDA;
     }
     return launch_status(la::launch_extend_wide(p, s));

@@ -288,6 +288,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Segment start states from the block states, in place.  With T_{-1} = S0 and every block of
+// blk_len tokens, T_k = e^{-s blk_len} T_{k-1} + B_k is the state after block k (the same sum the
+// segments would otherwise form term by term), and segment g starts from T_{g P - 1}, P blocks per
+// segment; the kernel overwrites block state g P - 1 with it, so that a segment's prologue reads
+// one matrix however far into the request it starts.  Four CTAs of 1024 threads per (request,
+// head), one float4 of the 128 x 128 state per thread: the scan is elementwise, and each thread
+// keeps eight block states' loads in flight ahead of its multiply-adds, so the serial chain over
+// the blocks costs one L2 round trip per eight blocks.
+constexpr int kScanThreads = 1024;
+constexpr int kScanAhead = 8;
+
+__global__ void __launch_bounds__(kScanThreads) state_scan_kernel(const ExtendParams p) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = p.Hkv;
+    const int part = blockIdx.x & 3;
+    const int bh = blockIdx.x >> 2;
+    const int h = bh % H;
+    const int b = bh / H;
+    const int slot = p.state_idx[b];
+    const int t0 = p.cu_seqlens[b];
+    const int t1 = p.cu_seqlens[b + 1];
+    if (slot < 0 || slot >= p.num_slots || t0 < 0 || t1 < t0 || t1 > p.T) return;  // reported by
+    const int n = t1 - t0;                                                         // the extend
+    if (n > p.max_seqlen) return;                                                   // kernel
+    const int nseg_b = (n + p.seg_len - 1) / p.seg_len;
+    if (nseg_b <= 1) return;
+    const int per_seg = p.seg_len / p.blk_len;
+    const int nk = (nseg_b - 1) * per_seg;  // blocks before the last segment
+    constexpr int kVec = kHeadDim * kHeadDim / 4;  // float4 per state
+    float4 *ws = reinterpret_cast<float4 *>(p.ws + ((size_t)b * H + h) * (size_t)(1 + p.nblk) *
+                                                       (kHeadDim * kHeadDim));
+    const int e = part * kScanThreads + threadIdx.x;
+    const float d = expf(-p.slopes[h] * (float)p.blk_len);
+    float4 t = __ldcg(ws + e);  // S0
+    for (int k0 = 0; k0 < nk; k0 += kScanAhead) {
+        float4 bk[kScanAhead];
+#pragma unroll
+        for (int j = 0; j < kScanAhead; ++j)
+            if (k0 + j < nk) bk[j] = __ldcg(ws + (size_t)(1 + k0 + j) * kVec + e);
+#pragma unroll
+        for (int j = 0; j < kScanAhead; ++j) {
+            const int k = k0 + j;
+            if (k < nk) {
+                t.x = fmaf(d, t.x, bk[j].x);
+                t.y = fmaf(d, t.y, bk[j].y);
+                t.z = fmaf(d, t.z, bk[j].z);
+                t.w = fmaf(d, t.w, bk[j].w);
+                if ((k + 1) % per_seg == 0) ws[(size_t)(1 + k) * kVec + e] = t;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // Split only when the batch leaves SMs idle: with u = B * H * 2 extend CTAs (two v blocks per
@@ -356,6 +410,13 @@ cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *orde
     if (B <= 0) return cudaSuccess;
     return launch_pdl(rank_requests_kernel, dim3((unsigned)((B + 255) / 256)), dim3(256), 0, stream,
                       cu_seqlens, B, order);
+}
+
+cudaError_t launch_state_scan(const ExtendParams &p, cudaStream_t stream) {
+    if (p.seg_len <= 0 || p.nblk <= 0) return cudaSuccess;
+    const long long ctas = (long long)p.B * p.Hkv * 4;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    return launch_pdl(state_scan_kernel, dim3((unsigned)ctas), dim3(kScanThreads), 0, stream, p);
 }
 
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream) {

@@ -563,35 +563,21 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
                 const int col0 = col_base + sub * 32;
                 float S[32];
                 if (split || p.group > 1) {
-                    // S = e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, from
-                    // the workspace the block-state kernel filled (the S0 copy alone for an
-                    // unsplit request of a grouped call).
-                    const float *w0 = p.ws + ((size_t)b * Hkv + hk) * (size_t)(1 + p.nblk) *
+                    // From the workspace: S0 (its copy) for the first segment and for an unsplit
+                    // request of a grouped call; for segment g >= 1 the start state
+                    // e^{-s g seg} S0 + sum_{k < g P} e^{-s (g seg - (k+1) blk)} B_k, which the
+                    // state scan left in block state g P - 1.
+                    const size_t m = g == 0 ? 0 : (size_t)g * (p.seg_len / p.blk_len);
+                    const float *w0 = p.ws + (((size_t)b * Hkv + hk) * (size_t)(1 + p.nblk) + m) *
                                                  (kHeadDim * kHeadDim) +
                                       (size_t)i * kHeadDim + c0 + col0;
-                    const float d0 = expf(-slope * (float)g * (float)p.seg_len);
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
                         const float4 f = reinterpret_cast<const float4 *>(w0)[x];
-                        S[4 * x] = d0 * f.x;
-                        S[4 * x + 1] = d0 * f.y;
-                        S[4 * x + 2] = d0 * f.z;
-                        S[4 * x + 3] = d0 * f.w;
-                    }
-                    const int nb = split ? g * (p.seg_len / p.blk_len) : 0;
-                    for (int kb = 0; kb < nb; ++kb) {
-                        const float dk =
-                            expf(-slope * (float)(g * p.seg_len - (kb + 1) * p.blk_len));
-                        const float4 *wk = reinterpret_cast<const float4 *>(
-                            w0 + (size_t)(1 + kb) * (kHeadDim * kHeadDim));
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) {
-                            const float4 f = wk[x];
-                            S[4 * x] = fmaf(dk, f.x, S[4 * x]);
-                            S[4 * x + 1] = fmaf(dk, f.y, S[4 * x + 1]);
-                            S[4 * x + 2] = fmaf(dk, f.z, S[4 * x + 2]);
-                            S[4 * x + 3] = fmaf(dk, f.w, S[4 * x + 3]);
-                        }
+                        S[4 * x] = f.x;
+                        S[4 * x + 1] = f.y;
+                        S[4 * x + 2] = f.z;
+                        S[4 * x + 3] = f.w;
                     }
                 } else if (p.prefix_mask[b]) {
 #pragma unroll

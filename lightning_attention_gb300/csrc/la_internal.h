@@ -106,12 +106,14 @@ struct ExtendParams {
     // segments of seg_len tokens, processed by separate CTAs; segment g starts from
     // e^{-s g seg_len} S0 + sum over the blocks k before it of e^{-s (g seg_len - (k+1) blk_len)} B_k,
     // where B_k is block k's local end state (blk_len tokens, from zero) and S0 the initial state,
-    // both written to the workspace by the block-state kernel beforehand.
+    // both written to the workspace by the block-state kernel beforehand; the state scan then
+    // leaves that start state in block state g P - 1 (P = seg_len / blk_len).
     int seg_len;   // multiple of blk_len
     int blk_len;   // multiple of the chunk length
     int nseg;      // segments per request, upper bound over the batch
     int nblk;      // blocks per request kept in the workspace
-    float *ws;     // [B][Hkv][1 + nblk][D][D]: S0 copy, then block states
+    float *ws;     // [B][Hkv][1 + nblk][D][D]: S0 copy, then block states (segment start states
+                   // at every P-th after the scan)
     int lpt;       // nonzero: CTAs take requests longest first (ranked on the device)
     // With lpt: the requests in decreasing length order (ties by index), written by the ranking
     // pre-pass into the workspace for large batches; null: every CTA ranks the (few) requests
@@ -147,6 +149,10 @@ bool make_token_map_full(CUtensorMap *m, const void *ptr, int T, int H);
 // The pre-pass of a split or grouped extend: the workspace copy of each initial state, and the
 // block states of split requests (la_extend_seg.cu).  Launched when p.seg_len > 0 or p.group > 1.
 cudaError_t launch_block_states(const ExtendParams &p, cudaStream_t stream);
+// The scan between the two: each split request's block states become, in place, the start states
+// of its segments (block g P - 1 holds segment g's), so that the extend kernel reads one matrix per
+// segment.  Launched after launch_block_states whenever p.seg_len > 0.
+cudaError_t launch_state_scan(const ExtendParams &p, cudaStream_t stream);
 // Longest-first order of a batch's requests: order[rank] = request, ranks by decreasing length,
 // ties by index (la_extend_seg.cu).  One thread per request compares it with every other.
 cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *order,
