@@ -310,9 +310,11 @@ class GpuCase:
                     self.launches_per_step = 2
                     self.kernel = "rank_requests_kernel + extend_wide_kernel (one la_extend call)"
                 else:
-                    # long requests split into segments: block-state kernel, then the extend kernel
-                    self.launches_per_step = 2
-                    self.kernel = "block_state_kernel + extend_wide_kernel (one la_extend call)"
+                    # long requests split into segments: block-state kernel, state scan, then
+                    # the extend kernel
+                    self.launches_per_step = 3
+                    self.kernel = ("block_state_kernel + state_scan_kernel + extend_wide_kernel "
+                                   "(one la_extend call)")
             self.track = None
             if w.track_lens is not None:
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
