@@ -64,3 +64,11 @@ def test_mixed_long_and_short_requests():
 @pytest.mark.parametrize("n", [2048, 2049, 4096, 6143, 8192, 8193])
 def test_lengths_around_segment_boundaries(n):
     check_split(workloads.custom_extend([n], H=1, prefix=[1], seed=n))
+
+
+@pytest.mark.parametrize("lengths,H", [([40000], 1), ([20000, 3000], 2)])
+def test_many_segments_few_heads(lengths, H):
+    # one or two heads per request leave the SMs to the segments: dozens of them, so the state
+    # scan between the two launches runs over many blocks (several rounds of its prefetch)
+    check_split(workloads.custom_extend(lengths, H=H, prefix=[1] * len(lengths), layer_id=2, L=5,
+                                        seed=sum(lengths) + H))
