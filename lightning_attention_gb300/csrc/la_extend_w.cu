@@ -111,8 +111,10 @@ constexpr uint32_t OFF_V = OFF_K + 2 * SZ_T;        // V of the chunk in flight 
 constexpr uint32_t OFF_KLO = OFF_V + SZ_T;          // lo half of lambda K (bf16)
 constexpr uint32_t OFF_SHI = OFF_KLO + SZ_T;
 constexpr uint32_t OFF_SLO = OFF_SHI + SZ_T;
-constexpr uint32_t OFF_TAB = OFF_SLO + SZ_T;        // e^{-s m}, m = 0..C
-constexpr uint32_t OFF_TABP = OFF_TAB + 544;        // e^{-s m} D^-0.5, m = 0..C
+// e^{-s m} and e^{-s m} D^-0.5 for m = 0..C: read per element only by the P blocks of steep
+// decays (slopes above kRunMaxSlope); every other factor is formed in registers
+constexpr uint32_t OFF_TAB = OFF_SLO + SZ_T;
+constexpr uint32_t OFF_TABP = OFF_TAB + 544;
 constexpr uint32_t OFF_BAR = OFF_TABP + 544;
 constexpr uint32_t SZ_BAR = 256;
 constexpr uint32_t kSmemBytes = OFF_BAR + SZ_BAR + 1024;  // + alignment slack
@@ -240,7 +242,7 @@ __device__ __forceinline__ void p_block(int i, int cb, const uint32_t (&v)[32], 
                                         uint32_t (&pl)[16]) {
     const int d = i - cb * 32;  // i - j for jj = 0; 0 <= d <= 127 for blocks on or below the diagonal
     if (run) {
-        float f = f0;  // tabp[d], read by the caller once per kernel
+        float f = f0;  // e^{-s d} D^-0.5, formed by the caller once per kernel
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 2) {
             const float f1 = f * g;
@@ -557,7 +559,7 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
                         (size_t)(c0 + col_base);
         {
             const int r0 = nchunks > 0 ? chunk_len(kEx, 0, sp, n) : 0;
-            const float d0s = tab[r0];  // 1 when there is no chunk
+            const float d0s = expf(-slope * (float)r0);
 #pragma unroll 1
             for (int sub = 0; sub < nsubs; ++sub) {
                 const int col0 = col_base + sub * 32;
@@ -614,17 +616,19 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
         const size_t head_stride = kEx ? (size_t)p.out_hs : (size_t)kHeadDim;
         bool ok = true;
         int cs_next = 0;
-        // Table values that stay fixed for every full chunk, read once: table reads inside the
-        // chunk are slow while the MMAs stream their operands.
-        const float gam = tabp[i + 1];     // gamma_i D^-0.5
-        const float dn_full = tab[C];      // decay over a full chunk
+        // Factors that stay fixed for every full chunk, formed once in registers (a ragged chunk
+        // forms its own): reading them from the table measured slower.
+        const float gam = expf(-slope * (float)(i + 1)) * kScale;  // gamma_i D^-0.5
+        const float dn_full = expf(-slope * (float)C);            // decay over a full chunk
         LamSplitBf lam_full[kKUnits];      // lambda of this warp's K units' rows, full chunk
 #pragma unroll
         for (int k = 0; k < kKUnits; ++k)
-            lam_full[k] = lam_split_bf16(tab[C - 1 - (((ku0 + k) >> 2) * 32 + lane)]);
+            lam_full[k] =
+                lam_split_bf16(expf(-slope * (float)(C - 1 - (((ku0 + k) >> 2) * 32 + lane))));
         // P start factors e^{-s (i - 32 cb)} D^-0.5 of this warp's (at most two) blocks
-        const float f_p0 = pb0 < pb1 ? tabp[i - 32 * pb0] : 0.f;
-        const float f_p1 = pb0 + 1 < pb1 ? tabp[i - 32 * (pb0 + 1)] : 0.f;
+        const float f_p0 = pb0 < pb1 ? expf(-slope * (float)(i - 32 * pb0)) * kScale : 0.f;
+        const float f_p1 =
+            pb0 + 1 < pb1 ? expf(-slope * (float)(i - 32 * (pb0 + 1))) * kScale : 0.f;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1;
             // first token of the chunk and its length
@@ -657,7 +661,8 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
 #pragma unroll
                 for (int k = 0; k < kKUnits; ++k) {
                     const LamSplitBf lam = r == C ? lam_full[k]
-                                                  : lam_split_bf16(rr[k] < r ? tab[r - 1 - rr[k]] : 0.f);
+                                                  : lam_split_bf16(rr[k] < r ? expf(-slope * (float)(r - 1 - rr[k]))
+                                                                             : 0.f);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         uint4 hi, lo;
@@ -706,7 +711,9 @@ __device__ __forceinline__ void extend_cta(const CUtensorMap &tq, const CUtensor
             tc_fence_after();
             {
                 const int r_next = c + 1 < nchunks ? chunk_len(kEx, cs + r, sp, n) : 0;
-                const float dn = c + 1 >= nchunks ? 1.f : r_next == C ? dn_full : tab[r_next];
+                const float dn = c + 1 >= nchunks ? 1.f
+                                 : r_next == C   ? dn_full
+                                                 : expf(-slope * (float)r_next);
 #pragma unroll 1
                 for (int sub = 0; sub < nsubs; ++sub) {
                     const int col0 = col_base + sub * 32;
