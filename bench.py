@@ -13,8 +13,8 @@ A step is one call of the path over one batch of the chosen workload (inputs res
   verify_tree    the same requests with an 8-token binary draft tree each
   varlen_extend_tracked  varlen_extend plus a state-tracking snapshot per request
   verify_commit  verify followed by the accepted-state commit (two library calls)
-  varlen_extend_b1024  1024 requests, lengths uniform in [32, 512], H=16 (longest first through
-                 the ranking pre-pass; also timed in index order)
+  varlen_extend_b1024  1024 requests, lengths uniform in [32, 512], H=16 (the persistent grid,
+                 longest first; also timed without a workspace: one CTA per (request, head))
 Every workload's inputs exceed the 129 MB L2, so no flush is needed between steps.  With N > 1
 (torchrun), every rank runs its own replica of the workload (weak scaling, no collective on the
 data path); timing is bracketed by a barrier and the slowest rank's time is reported.
@@ -65,7 +65,7 @@ KERNEL_SOURCE = {
     "verify_tree": "la_recurrent.cu",
     "varlen_extend_tracked": "la_extend_w.cu",
     "verify_commit": "la_recurrent.cu",
-    "varlen_extend_b1024": ("la_extend_w.cu", "la_extend_seg.cu"),
+    "varlen_extend_b1024": "la_extend_many.cu",
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
@@ -75,7 +75,7 @@ KERNEL_NAME = {
     "verify_tree": "recurrent_kernel<3>",
     "varlen_extend_tracked": "extend_wide_kernel",
     "verify_commit": "recurrent_kernel<1>",
-    "varlen_extend_b1024": "extend_wide_kernel",
+    "varlen_extend_b1024": "extend_many_kernel",
 }
 # Small cases of the same kernels for multi-pass ncu captures (--profile-calls); a few GB at most.
 PROFILE_CASES = {
@@ -304,8 +304,14 @@ class GpuCase:
             lens = w.cu_seqlens[1:] - w.cu_seqlens[:-1]
             self.max_seqlen = int(lens.max()) if w.B else 0
             self.workspace = None  # the binding supplies what la_extend_workspace_size asks for
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
             if la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen) > 0:
-                if w.B > 256:
+                if w.B * w.H > sms:
+                    # more (request, head) pairs than SMs: the request-record pre-pass, then the
+                    # persistent grid
+                    self.launches_per_step = 2
+                    self.kernel = "item_records_kernel + extend_many_kernel (one la_extend call)"
+                elif w.B > 256:
                     # a large batch: the ranking pre-pass, then the extend kernel
                     self.launches_per_step = 2
                     self.kernel = "rank_requests_kernel + extend_wide_kernel (one la_extend call)"
@@ -319,7 +325,8 @@ class GpuCase:
             if w.track_lens is not None:
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
                 self.kernel = self.kernel.replace("extend_wide_kernel",
-                                                  "extend_wide_kernel<true>")
+                                                  "extend_wide_kernel<true>").replace(
+                                                      "extend_many_kernel", "extend_many_kernel<true>")
         if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
         if w.kind == "tree":
@@ -440,7 +447,8 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
         case.workspace = None
         case.launches_per_step += 1
         index_order = {"ms_per_step": round(max_over_ranks(io_s, world, dev) / steps * 1e3, 4),
-                       "note": "requests in index order instead of longest first"}
+                       "note": "without a workspace: one CTA per (request, head), requests in "
+                               "index order"}
 
     e2e = None
     if with_e2e:

@@ -113,7 +113,10 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *                contents on entry do not matter and are garbage on exit; calls sharing one
  *                workspace must not overlap on the GPU.  Without the sequence split, SMs left
  *                idle may take the longest requests as two CTAs per head (la_set_column_split);
- *                that needs no scratch.
+ *                that needs no scratch.  A batch of more (request, head) pairs than SMs runs on
+ *                a persistent grid of one CTA per SM (la_set_persistent), which keeps B records
+ *                of 32 bytes in the workspace; without them it runs one CTA per pair, in waves
+ *                (same results, bit for bit).
  *   workspace_bytes  size of workspace
  *   stream       cudaStream_t
  * Numerics: bf16 inputs; fp32 states and accumulation.  Every product runs on the tensor cores
@@ -171,7 +174,9 @@ la_status la_extend_ex(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, con
 
 /*
  * la_extend_workspace_size -- bytes of device scratch la_extend would use for a batch of this
- * shape on the current device (0 when it would not split any request).  Host only, no device work
+ * shape on the current device: the block states of a sequence split, the longest-first order of a
+ * batch of more than 256 requests, the request records of the persistent grid (0 when it needs
+ * none of these).  Host only, no device work
  * beyond one cached attribute query.  Arguments as for la_extend; *bytes is written on success.
  * Returns LA_ERR_INVALID for negative sizes or bytes == NULL, LA_ERR_UNSUPPORTED for D != 128.
  */
@@ -363,6 +368,18 @@ void la_set_wait_limit(uint64_t microseconds);
  * Host only; applies to later launches from this process.
  */
 void la_set_column_split(int enable);
+
+/*
+ * la_set_persistent -- scheduling switch for la_extend / la_extend_ex (default 1: on).  A batch
+ * whose B * H (request, head) pairs outnumber the device's SMs runs, when the workspace has room
+ * for its request records, on a persistent grid: one CTA per SM works through its share of the
+ * pairs (longest first, dealt in snake order), keeping its barriers and tensor memory and loading
+ * the next pair's tiles while it finishes the current one.  Every pair is computed as one CTA per
+ * pair computes it, so the results are bit-identical either way.  0 runs one CTA per pair always.
+ * Grouped-query calls always run one CTA per pair.  Host only; applies to later launches from
+ * this process.
+ */
+void la_set_persistent(int enable);
 
 #ifdef __cplusplus
 }

@@ -27,6 +27,7 @@ std::mutex g_mutex;
 unsigned int *g_err_ptr[kMaxDevices] = {nullptr};
 std::atomic<unsigned long long> g_wait_limit{0};
 std::atomic<int> g_column_split{1};
+std::atomic<int> g_persistent{1};
 
 // Default bound on a device wait: far above any legitimate wait inside one CTA (microseconds),
 // short enough that a lost arrival ends the kernel in about two seconds instead of hanging.
@@ -101,6 +102,8 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out) {
 void la_set_wait_limit(uint64_t microseconds) { g_wait_limit.store(microseconds); }
 
 void la_set_column_split(int enable) { g_column_split.store(enable ? 1 : 0); }
+
+void la_set_persistent(int enable) { g_persistent.store(enable ? 1 : 0); }
 
 la_status la_poll_error(la_stream stream) {
     // The error word is per device, so every kernel that may write it -- on any stream of the
@@ -256,6 +259,8 @@ struct ExtendScratch {
     unsigned long long copies; // bytes of the initial-state copies alone (grouped calls)
     unsigned long long order;  // bytes of the longest-first order array (large batches), after
                                // `full`
+    unsigned long long recs;   // bytes of the persistent extend's request records (batches of
+                               // more than one wave), after the order array
 };
 
 // Up to this many requests every extend CTA ranks the batch itself; above it, a pre-pass ranks
@@ -263,7 +268,7 @@ struct ExtendScratch {
 constexpr int kInCtaRankedRequests = 256;
 
 la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScratch *out) {
-    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull, 0ull};
+    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull, 0ull, 0ull};
     const unsigned long long mat = (unsigned long long)la::kHeadDim * la::kHeadDim * sizeof(float);
     if (Hkv < H) out->copies = (unsigned long long)B * Hkv * mat;
     out->full = out->copies;
@@ -273,6 +278,8 @@ la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScr
     int sms = 0;
     la_status st = num_sms(&sms);
     if (st != LA_OK) return st;
+    if (Hkv == H && (long long)B * H > sms && B <= la::kMaxRankedRequests)
+        out->recs = (unsigned long long)B * sizeof(la::ItemRec);
     const la::SplitPlan pl = la::plan_split(B, H, max_seqlen, sms, kExtendCtasPerHead);
     if (pl.seg_len > 0) {
         out->plan = pl;
@@ -366,6 +373,18 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         p.order = order;
         p.lpt = 1;
     }
+    // Persistent grid: a batch of more (request, head) pairs than SMs runs on one CTA per SM
+    // when the workspace has room for the request records.
+    la::ItemRec *recs = nullptr;
+    int many_ctas = 0;
+    if (workspace != nullptr && scr.recs > 0 && g_persistent.load() &&
+        (unsigned long long)workspace_bytes >= scr.full + scr.order + scr.recs) {
+        int sms = 0;
+        if ((st = num_sms(&sms)) != LA_OK) return st;
+        recs = reinterpret_cast<la::ItemRec *>(static_cast<char *>(workspace) + scr.full +
+                                               scr.order);
+        many_ctas = sms;
+    }
     // Column split: SMs that one CTA per (request, head) leaves idle take the second value-column
     // half of the longest requests, H CTAs per request.
     p.csplit = 0;
@@ -376,6 +395,9 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
         if (spare >= H) p.csplit = (int)std::min<long long>(B, spare / H);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.recs = nullptr;
+    if (many_ctas > 0 && p.seg_len == 0 && p.csplit == 0 && p.group == 1)
+        return launch_status(la::launch_extend_many(p, recs, many_ctas, s));
     if (order != nullptr && la::launch_rank_requests(cu_seqlens, B, order, s) != cudaSuccess)
         return LA_ERR_CUDA;
     if (p.seg_len > 0 || p.group > 1) {
@@ -419,7 +441,7 @@ la_status la_extend_gqa_workspace_size(int B, int T, int H, int Hkv, int D, int 
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, Hkv, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)(scr.full + scr.order);
+    *bytes = (size_t)(scr.full + scr.order + scr.recs);
     return LA_OK;
 }
 
@@ -474,7 +496,7 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, H, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)(scr.full + scr.order);
+    *bytes = (size_t)(scr.full + scr.order + scr.recs);
     return LA_OK;
 }
 

@@ -18,10 +18,12 @@
 // reason: the group's first query head rewrites the slot that its siblings start from.
 //
 // One CTA per (request, head, block): a TMA warp streams the block's K and V tiles (C x 128 each,
-// three stages); eight warps scale K by e^{-s (e - 1 - t)} into a bf16 pair hi (in place) + lo;
-// one thread issues tcgen05.mma (bf16 x bf16 -> fp32) accumulating B = K_hi^T V + K_lo^T V in
-// tensor memory over the whole block, V straight from the TMA tile; the eight warps then write B
-// (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so one
+// three stages), last chunk first: the extend kernel starts each segment at its first chunk, so
+// the tiles read last here are the first it reads again, while some are still in L2 (the terms
+// of B do not depend on the order they are summed in).  Eight warps scale K by e^{-s (e - 1 - t)}
+// into a bf16 pair hi (in place) + lo; one thread issues tcgen05.mma (bf16 x bf16 -> fp32)
+// accumulating B = K_hi^T V + K_lo^T V in tensor memory over the whole block, V straight from the
+// TMA tile; the eight warps then write B (fp32, 64 KiB) to the workspace.  The decay factors of a block span its whole length, so one
 // 16-bit K_hat would round every term by up to 2^-9 (bf16) or 2^-11 (fp16), an error that the
 // state of a slowly decaying head sums over thousands of tokens; the pair keeps the terms to
 // about 2^-17.  The work is HBM bound (64 KiB of K and V per 128 tokens, 4 x 128 x 128 x 128 MMA
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c >= kStages && !wait_bar(&bars->empty[st], (c / kStages - 1) & 1, limit,
                                               abort_flag, p.err))
                     break;
-                const int y = t0 + a + c * C;
+                const int y = t0 + a + (nchunks - 1 - c) * C;  // last chunk first
                 const int x = h * kHeadDim;
                 uint8_t *dst = sm + st * SZ_STAGE;
                 mbar_arrive_expect_tx(&bars->full[st], SZ_STAGE);
@@ -230,9 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait_bar(&bars->full[st], (c / kStages) & 1, limit, abort_flag,
                                      p.err)))
                 break;
-            // distance of this token to the block's last token: (blk_len - 1) - (c C + row)
+            // distance of this token to the block's last token: (blk_len - 1) - (cc C + row), where
+            // cc = nchunks - 1 - c is the chunk's place in the block
+            const int cc = nchunks - 1 - c;
             const LamSplitBf lam =
-                lam_split_bf16(expf(-slope * (float)(p.blk_len - 1 - c * C - row)));
+                lam_split_bf16(expf(-slope * (float)(p.blk_len - 1 - cc * C - row)));
             uint4 *krow = reinterpret_cast<uint4 *>(sm + st * SZ_STAGE + half * 16384 + row * 128);
             uint4 *lrow = reinterpret_cast<uint4 *>(sm + OFF_KLO + half * 16384 + row * 128);
             const int rot = row + half * 4;  // 8 threads of a quarter-warp hit 8 distinct banks
@@ -377,10 +381,7 @@ SplitPlan plan_split(int B, int H, int max_seqlen, int num_sms, int ctas_per_hea
 
 namespace {
 
-// order[rank of b] = b, the rank of request b being the number of requests that are longer, or
-// as long with a smaller index: a strict total order, so the ranks are a permutation even for
-// inconsistent cu_seqlens (which the extend kernel reports).  The lengths are staged through
-// shared memory 256 at a time.
+// order[rank of b] = b, ranks by decreasing length (request_rank).
 __global__ void __launch_bounds__(256) rank_requests_kernel(const int32_t *cu_seqlens, int B,
                                                             int32_t *order) {
     pdl_wait();
@@ -388,18 +389,7 @@ __global__ void __launch_bounds__(256) rank_requests_kernel(const int32_t *cu_se
     __shared__ int lens[256];
     const int b = blockIdx.x * 256 + threadIdx.x;
     const int lb = b < B ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
-    int rank = 0;
-    for (int u0 = 0; u0 < B; u0 += 256) {
-        __syncthreads();
-        const int u = u0 + threadIdx.x;
-        lens[threadIdx.x] = u < B ? cu_seqlens[u + 1] - cu_seqlens[u] : 0;
-        __syncthreads();
-        const int m = min(256, B - u0);
-        for (int x = 0; x < m; ++x) {
-            const int lu = lens[x];
-            rank += (lu > lb) || (lu == lb && u0 + x < b);
-        }
-    }
+    const int rank = request_rank(cu_seqlens, B, b, lb, lens);
     if (b < B) order[rank] = b;
 }
 

@@ -22,6 +22,28 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Rank of request b (length lb) in decreasing length order: the number of the B requests that
+// are longer, or as long with a smaller index.  A strict total order, so the ranks are a
+// permutation even for inconsistent cu_seqlens (which the extend kernels report).  Every thread
+// of the 256-thread block calls it (b past B too); the lengths are staged through `lens` 256 at
+// a time.
+__device__ __forceinline__ int request_rank(const int32_t *cu_seqlens, int B, int b, int lb,
+                                            int (&lens)[256]) {
+    int rank = 0;
+    for (int u0 = 0; u0 < B; u0 += 256) {
+        __syncthreads();
+        const int u = u0 + threadIdx.x;
+        lens[threadIdx.x] = u < B ? cu_seqlens[u + 1] - cu_seqlens[u] : 0;
+        __syncthreads();
+        const int m = B - u0 < 256 ? B - u0 : 256;
+        for (int x = 0; x < m; ++x) {
+            const int lu = lens[x];
+            rank += (lu > lb) || (lu == lb && u0 + x < b);
+        }
+    }
+    return rank;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args &&...args) {
@@ -85,6 +107,14 @@ struct CommitParams {
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t stream);
 
 // Chunked tensor-core extend (tcgen05 + TMA), one CTA per (request, head, segment).
+// A request's geometry for the persistent extend kernel; the heads of the request share it.
+struct alignas(16) ItemRec {
+    int b, t0, n, slot;             // request, first token, length, pool slot
+    int sp, tslot, nchunks, flags;  // tracked token (n + 1: none) and its slot; chunks; kRec*
+};
+constexpr int kRecValid = 1;   // a request without faults (the others are skipped)
+constexpr int kRecPrefix = 2;  // starts from its pool slot (else from zero)
+
 struct ExtendParams {
     const __nv_bfloat16 *q, *k, *v;
     const float *slopes;
@@ -123,6 +153,8 @@ struct ExtendParams {
     // two CTAs per head, one per 64-column half of the values, which shortens their chunk chains
     // when the batch leaves SMs idle; the grid has (B + csplit) H CTAs.
     int csplit;
+    // Persistent extend: the requests' geometry in decreasing length order (null otherwise).
+    const ItemRec *recs;
     // State tracking (both null: none).  For b with track_lens[b] >= 0 the state after the first
     // track_lens[b] tokens of the request is also written to slot track_idx[b]; the CTA that
     // holds that token restarts its chunk grid there and stores the state at that boundary.
@@ -159,5 +191,12 @@ cudaError_t launch_rank_requests(const int32_t *cu_seqlens, int B, int32_t *orde
                                  cudaStream_t stream);
 // Batches above this size keep index order (the ranking's work grows as B^2).
 constexpr int kMaxRankedRequests = 65536;
+
+// Persistent extend for batches of more than one wave (la_extend_many.cu): a pre-pass writes one
+// ItemRec per request into recs (B of them, in decreasing length order, reporting each faulty
+// request once), then `ctas` CTAs work through the (request, head) pairs.  Only for p.group == 1
+// without a sequence or column split.
+cudaError_t launch_extend_many(const ExtendParams &p, ItemRec *recs, int ctas,
+                               cudaStream_t stream);
 
 }  // namespace la

@@ -88,6 +88,11 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// Prefetch the cache line holding global address p into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p)) : "memory");
+}
+
 // 2D tiled store of one box from shared memory (128-byte swizzled, as the tensor map says) to
 // global memory, tracked by this thread's bulk async-group.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *smem_src, int x, int y) {
