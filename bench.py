@@ -81,6 +81,8 @@ KERNEL_NAME = {
 PROFILE_CASES = {
     "verify_b32": lambda: workloads.verify_chain(0, B=32, num_slots=64),
     "verify_tree_b32": lambda: workloads.verify_tree(0, B=32, num_slots=64),
+    # a quarter of the 1024-request batch: still 4,096 (request, head) pairs, the persistent grid
+    "extend_many_b256": lambda: workloads.varlen_extend_many(0, B=256, num_slots=512),
 }
 
 
