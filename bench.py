@@ -786,7 +786,8 @@ def main_profile(args):
     torch.cuda.set_device(dev)
     if args.profile_case:
         w, name = PROFILE_CASES[args.profile_case](), args.profile_case
-        kname = {"verify_b32": "verify", "verify_tree_b32": "verify_tree"}[name]
+        kname = {"verify_b32": "verify", "verify_tree_b32": "verify_tree",
+                 "extend_many_b256": "varlen_extend_b1024"}[name]
     else:
         w, name = make_workload(args.workload, 0), args.workload
         kname = name
