@@ -116,7 +116,14 @@ la_status la_slopes(int H, int layer_id, int L, float *host_out);
  *                that needs no scratch.  A batch of more (request, head) pairs than SMs runs on
  *                a persistent grid of one CTA per SM (la_set_persistent), which keeps B records
  *                of 32 bytes in the workspace; without them it runs one CTA per pair, in waves
- *                (same results, bit for bit).
+ *                (same results, bit for bit).  A batch of 2 .. 256 requests whose B * H pairs fit
+ *                on the SMs, that has no sequence split and whose max_seqlen is at least twice
+ *                its mean length T / B, runs balanced when the workspace has room for its plan
+ *                (la_set_balanced): a one-block planner on the device cuts the
+ *                longest requests into segments from their actual lengths, each segment's CTA
+ *                first forms its start state from the request's earlier keys and values, and a
+ *                persistent grid of one CTA per SM works through the segments (about 13 KiB of
+ *                plan in the workspace; same results up to rounding).
  *   workspace_bytes  size of workspace
  *   stream       cudaStream_t
  * Numerics: bf16 inputs; fp32 states and accumulation.  Every product runs on the tensor cores
@@ -380,6 +387,20 @@ void la_set_column_split(int enable);
  * this process.
  */
 void la_set_persistent(int enable);
+
+/*
+ * la_set_balanced -- scheduling switch for la_extend / la_extend_ex (default 1: on).  A batch of
+ * 2 .. 256 requests whose B * H (request, head) pairs fit on the device's SMs, that has no
+ * sequence split and whose max_seqlen is at least twice its mean length T / B (a few long
+ * requests among short ones), runs, when the workspace has room for the plan, as segments planned on the
+ * device: the longest requests are cut so that every SM gets about the same number of chunks
+ * (each segment's CTA first forms the state at its start from the request's earlier keys and
+ * values, reading them a second time), and one CTA per SM works through the segments.  The
+ * result is the same up to rounding either way (the start state of a segment sums the same terms
+ * in another grouping).  0 keeps one CTA per (request, head), with the column split.  Grouped-
+ * query calls never run balanced.  Host only; applies to later launches from this process.
+ */
+void la_set_balanced(int enable);
 
 #ifdef __cplusplus
 }

@@ -6,5 +6,5 @@ and the seeded synthetic workloads (workloads.py).
 """
 from .binding import (LAError, commit_accepted, decode, decode_gqa, extend, extend_gqa,  # noqa
                       extend_gqa_workspace_size, extend_noalloc, extend_workspace_size, load,
-                      poll_error, set_column_split, set_persistent, set_wait_limit, slopes,
+                      poll_error, set_balanced, set_column_split, set_persistent, set_wait_limit, slopes,
                       verify_chain, verify_tree)

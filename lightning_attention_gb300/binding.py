@@ -26,7 +26,7 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_C
 
 EXPORTS = ("la_slopes", "la_extend", "la_extend_ex", "la_extend_workspace_size", "la_decode",
            "la_verify_chain", "la_verify_tree", "la_commit_accepted", "la_poll_error", "la_status_string",
-           "la_set_wait_limit", "la_set_column_split", "la_set_persistent", "la_extend_noalloc", "la_extend_gqa",
+           "la_set_wait_limit", "la_set_column_split", "la_set_persistent", "la_set_balanced", "la_extend_noalloc", "la_extend_gqa",
            "la_extend_gqa_workspace_size", "la_decode_gqa")
 
 
@@ -84,6 +84,8 @@ def load():
         lib.la_set_column_split.restype = None
         lib.la_set_persistent.argtypes = [ctypes.c_int]
         lib.la_set_persistent.restype = None
+        lib.la_set_balanced.argtypes = [ctypes.c_int]
+        lib.la_set_balanced.restype = None
         lib.la_extend_gqa.argtypes = [vp, vp, vp, vp, vp, ip, vp, vp, vp, vp, ip, ip, ip, ip, ip,
                                       ip, vp, sz, vp]
         lib.la_extend_gqa.restype = ip
@@ -183,6 +185,12 @@ def set_persistent(enable: bool) -> None:
     """Scheduling switch of the extend calls (on by default): a batch of more (request, head)
     pairs than SMs runs on a persistent grid of one CTA per SM; results are bit-identical."""
     load().la_set_persistent(1 if enable else 0)
+
+
+def set_balanced(enable: bool) -> None:
+    """Scheduling switch of the extend calls (on by default): a one-wave batch of uneven lengths
+    runs as segments planned on the device, on one CTA per SM; results agree up to rounding."""
+    load().la_set_balanced(1 if enable else 0)
 
 
 def poll_error(device=None) -> None:

@@ -28,6 +28,7 @@ unsigned int *g_err_ptr[kMaxDevices] = {nullptr};
 std::atomic<unsigned long long> g_wait_limit{0};
 std::atomic<int> g_column_split{1};
 std::atomic<int> g_persistent{1};
+std::atomic<int> g_balanced{1};
 
 // Default bound on a device wait: far above any legitimate wait inside one CTA (microseconds),
 // short enough that a lost arrival ends the kernel in about two seconds instead of hanging.
@@ -104,6 +105,8 @@ void la_set_wait_limit(uint64_t microseconds) { g_wait_limit.store(microseconds)
 void la_set_column_split(int enable) { g_column_split.store(enable ? 1 : 0); }
 
 void la_set_persistent(int enable) { g_persistent.store(enable ? 1 : 0); }
+
+void la_set_balanced(int enable) { g_balanced.store(enable ? 1 : 0); }
 
 la_status la_poll_error(la_stream stream) {
     // The error word is per device, so every kernel that may write it -- on any stream of the
@@ -261,14 +264,22 @@ struct ExtendScratch {
                                // `full`
     unsigned long long recs;   // bytes of the persistent extend's request records (batches of
                                // more than one wave), after the order array
+    unsigned long long bal;    // bytes of the balanced extend's plan (one-wave batches without a
+                               // sequence split), after the records
 };
+
+// A one-wave batch runs balanced when its longest request (max_seqlen) is at least this many times
+// the mean length T / B.  Balancing reads the keys and values before each cut a second time and
+// keeps every SM streaming, which slows each chunk (3.4-3.6 us against 3.05 us); on batches of
+// lengths within a factor of about two of each other the column split does as well or better.
+constexpr long long kBalancedSkew = 2;
 
 // Up to this many requests every extend CTA ranks the batch itself; above it, a pre-pass ranks
 // it once into the workspace.
 constexpr int kInCtaRankedRequests = 256;
 
 la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScratch *out) {
-    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull, 0ull, 0ull};
+    *out = ExtendScratch{la::SplitPlan{0, 0, 1, 0, 0ull}, 0ull, 0ull, 0ull, 0ull, 0ull};
     const unsigned long long mat = (unsigned long long)la::kHeadDim * la::kHeadDim * sizeof(float);
     if (Hkv < H) out->copies = (unsigned long long)B * Hkv * mat;
     out->full = out->copies;
@@ -284,6 +295,9 @@ la_status extend_scratch(int B, int T, int H, int Hkv, int max_seqlen, ExtendScr
     if (pl.seg_len > 0) {
         out->plan = pl;
         out->full = (unsigned long long)B * Hkv * (unsigned long long)(1 + pl.nblk) * mat;
+    } else if (Hkv == H && B >= 2 && B <= la::kMaxBalRequests && (long long)B * H <= sms &&
+               (long long)max_seqlen * B >= kBalancedSkew * (long long)T) {
+        out->bal = la::bal_scratch_bytes(B, H);
     }
     return LA_OK;
 }
@@ -396,6 +410,16 @@ la_status extend_impl(const la_bf16 *q, const la_bf16 *k, const la_bf16 *v, cons
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     p.recs = nullptr;
+    // Balanced grid: a one-wave batch whose requests differ in length runs as segments planned
+    // on the device, on one CTA per SM, when the workspace has room for the plan.
+    if (workspace != nullptr && scr.bal > 0 && g_balanced.load() && p.seg_len == 0 &&
+        p.group == 1 && T > 0 &&
+        (unsigned long long)workspace_bytes >= scr.full + scr.order + scr.recs + scr.bal) {
+        int sms = 0;
+        if ((st = num_sms(&sms)) != LA_OK) return st;
+        void *plan = static_cast<char *>(workspace) + scr.full + scr.order + scr.recs;
+        return launch_status(la::launch_extend_bal(p, plan, sms, s));
+    }
     if (many_ctas > 0 && p.seg_len == 0 && p.csplit == 0 && p.group == 1)
         return launch_status(la::launch_extend_many(p, recs, many_ctas, s));
     if (order != nullptr && la::launch_rank_requests(cu_seqlens, B, order, s) != cudaSuccess)
@@ -441,7 +465,7 @@ la_status la_extend_gqa_workspace_size(int B, int T, int H, int Hkv, int D, int 
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, Hkv, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)(scr.full + scr.order + scr.recs);
+    *bytes = (size_t)(scr.full + scr.order + scr.recs + scr.bal);
     return LA_OK;
 }
 
@@ -496,7 +520,7 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
     ExtendScratch scr;
     const la_status st = extend_scratch(B, T, H, H, max_seqlen, &scr);
     if (st != LA_OK) return st;
-    *bytes = (size_t)(scr.full + scr.order + scr.recs);
+    *bytes = (size_t)(scr.full + scr.order + scr.recs + scr.bal);
     return LA_OK;
 }
 

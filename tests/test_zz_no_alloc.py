@@ -115,7 +115,8 @@ def test_no_alloc_allocates_nothing():
 def test_no_alloc_matches_la_extend_on_unsplit_batch():
     w = workloads.custom_extend([300, 1, 129, 0], H=16, prefix=[1, 0, 1, 0], seed=32)
     a = _inputs(w)
-    assert la.extend_workspace_size(w.B, w.T, w.H, w.D, a["max_seqlen"]) == 0
+    # no sequence split: the only scratch is the balanced schedule's plan (a few KiB of records)
+    assert 0 < la.extend_workspace_size(w.B, w.T, w.H, w.D, a["max_seqlen"]) < 65536
     pool_ref = w.materialize_pool(DEV)
     out_ref = _extend(a, pool_ref)
     for call in range(2):
