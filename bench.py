@@ -15,6 +15,9 @@ A step is one call of the path over one batch of the chosen workload (inputs res
   verify_commit  verify followed by the accepted-state commit (two library calls)
   varlen_extend_b1024  1024 requests, lengths uniform in [32, 512], H=16 (the persistent grid,
                  longest first; also timed without a workspace: one CTA per (request, head))
+  varlen_extend_skewed  8 requests: two of 4096-8192 tokens, six of 256-1024, H=16 (the balanced
+                 schedule; also timed with it switched off: one CTA per (request, head) and the
+                 column split)
 Every workload's inputs exceed the 129 MB L2, so no flush is needed between steps.  With N > 1
 (torchrun), every rank runs its own replica of the workload (weak scaling, no collective on the
 data path); timing is bracketed by a barrier and the slowest rank's time is reported.
@@ -66,6 +69,7 @@ KERNEL_SOURCE = {
     "varlen_extend_tracked": "la_extend_w.cu",
     "verify_commit": "la_recurrent.cu",
     "varlen_extend_b1024": "la_extend_many.cu",
+    "varlen_extend_skewed": "la_extend_bal.cu",
 }
 KERNEL_NAME = {
     "decode": "recurrent_kernel<0>",
@@ -76,6 +80,7 @@ KERNEL_NAME = {
     "varlen_extend_tracked": "extend_wide_kernel",
     "verify_commit": "recurrent_kernel<1>",
     "varlen_extend_b1024": "extend_many_kernel",
+    "varlen_extend_skewed": "extend_bal_kernel",
 }
 # Small cases of the same kernels for multi-pass ncu captures (--profile-calls); a few GB at most.
 PROFILE_CASES = {
@@ -307,7 +312,8 @@ class GpuCase:
             self.max_seqlen = int(lens.max()) if w.B else 0
             self.workspace = None  # the binding supplies what la_extend_workspace_size asks for
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            if la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen) > 0:
+            nbytes = la.extend_workspace_size(w.B, w.T, w.H, D, self.max_seqlen)
+            if nbytes > 0:
                 if w.B * w.H > sms:
                     # more (request, head) pairs than SMs: the request-record pre-pass, then the
                     # persistent grid
@@ -317,6 +323,10 @@ class GpuCase:
                     # a large batch: the ranking pre-pass, then the extend kernel
                     self.launches_per_step = 2
                     self.kernel = "rank_requests_kernel + extend_wide_kernel (one la_extend call)"
+                elif nbytes < 65536:
+                    # a skewed one-wave batch: the plan on the device, then the balanced grid
+                    self.launches_per_step = 2
+                    self.kernel = "seg_plan_kernel + extend_bal_kernel (one la_extend call)"
                 else:
                     # long requests split into segments: block-state kernel, state scan, then
                     # the extend kernel
@@ -328,7 +338,8 @@ class GpuCase:
                 self.track = (w.track_lens.to(dev), w.track_idx.to(dev))
                 self.kernel = self.kernel.replace("extend_wide_kernel",
                                                   "extend_wide_kernel<true>").replace(
-                                                      "extend_many_kernel", "extend_many_kernel<true>")
+                                                      "extend_many_kernel", "extend_many_kernel<true>").replace(
+                                                      "extend_bal_kernel", "extend_bal_kernel<true>")
         if w.kind in ("verify", "tree"):
             self.inter = torch.empty((w.B, w.N, w.H, D, D), dtype=torch.float32, device=dev)
         if w.kind == "tree":
@@ -451,6 +462,18 @@ def time_gpu(name, steps, warmup, world, rank, dev, peaks, with_e2e=True, sample
         index_order = {"ms_per_step": round(max_over_ranks(io_s, world, dev) / steps * 1e3, 4),
                        "note": "without a workspace: one CTA per (request, head), requests in "
                                "index order"}
+    if "extend_bal_kernel" in case.kernel:
+        # the same batch with the balanced schedule switched off, for comparison
+        la.set_balanced(False)
+        saved = (case.kernel, case.launches_per_step)
+        case.launches_per_step = 1
+        case.step()
+        ub_s, _ = timed_region(case, steps, world, dev, stream)
+        la.set_balanced(True)
+        case.kernel, case.launches_per_step = saved
+        index_order = {"ms_per_step": round(max_over_ranks(ub_s, world, dev) / steps * 1e3, 4),
+                       "note": "balanced schedule off: one CTA per (request, head), the longest "
+                               "requests' value columns split over idle SMs"}
 
     e2e = None
     if with_e2e:
@@ -624,7 +647,7 @@ def run_oracle_sample(w, sample, threads):
 ORACLE_BUDGET = {  # (request, head) pairs or token-heads per sample: ~1-10 s of fp64 CPU work
     "decode": 4096, "verify": 64 * 5 * 16, "varlen_extend": 16 * 2400, "long_prefill": 32 * 1200,
     "verify_tree": 64 * 8 * 8, "varlen_extend_tracked": 16 * 2400, "verify_commit": 64 * 5 * 16,
-    "varlen_extend_b1024": 16 * 2400}
+    "varlen_extend_b1024": 16 * 2400, "varlen_extend_skewed": 16 * 2400}
 
 
 def cpu_baseline(name, w, threads):
@@ -743,8 +766,8 @@ def main():
 # The other workloads, each timed like the headline (3 repeats of up to 20 steps, clocks sampled
 # over them).  The chain verify of 128 x 5 draft tokens comes last so that it is in the tail of
 # the printed line.
-OTHER_ORDER = ("varlen_extend_b1024", "verify_tree", "varlen_extend_tracked", "verify_commit",
-               "varlen_extend", "long_prefill", "verify")
+OTHER_ORDER = ("varlen_extend_b1024", "varlen_extend_skewed", "verify_tree",
+               "varlen_extend_tracked", "verify_commit", "varlen_extend", "long_prefill", "verify")
 
 
 def compact_entry(r, steps, cpu):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "la.h"
+#include "la_extend_bal.h"
 #include "la_internal.h"
 
 namespace {

@@ -24,12 +24,13 @@
 // (loading its start state, writing its final state).
 // For a target item cost M, a request of n chunks is cut from its start: each segment takes as
 // many chunks as keep its cost within M, at least two, and a remainder shorter than two chunks
-// joins the segment before it; then the smallest target that cuts it into no more segments is
-// taken instead, which evens out its segments' costs.  Sixteen targets from the mean load per CTA up to the longest
-// request (no cut) are tried, one per warp.  For each, the segments' items (one per head) are put
+// joins the segment before it.  Sixteen targets from the mean load per CTA up to the longest
+// request (no cut) are tried on those cuts, one per warp.  For each, the segments' items (one per head) are put
 // in order -- the non-last segments of cut requests first, then the rest, each by decreasing cost
 // -- and dealt to the P CTAs in snake order (CTA j takes ranks j, 2P - 1 - j, 2P + j, ...); the
-// target with the smallest largest CTA load wins (ties: fewer segments).  Targets that need more
+// target with the smallest largest CTA load wins (ties: fewer segments).  Its requests are then cut
+// into as many segments as before with the smallest target that needs no more, which evens out
+// their costs and shortens the first segments, whose keys and values the later ones read again.  Targets that need more
 // than 2P items, or more than P items of non-last segments, are not taken.
 //
 // The initial state of a cut request.  Each segment of a request with a prefix reads S0 from the
@@ -52,6 +53,7 @@
 
 #include <mutex>
 
+#include "la_extend_bal.h"
 #include "la_extend_tile.cuh"
 
 namespace la {
@@ -94,7 +96,9 @@ __device__ __forceinline__ int cut_request(int nc, int M, int (&ends)[kMaxSegs])
     }
     const int m = cut_greedy(nc, M, nullptr);
     if (m > 1) {
-        int lo = 0, hi = M;  // cut_greedy(nc, hi) <= m throughout
+        // m segments cover nc chunks, so one of them costs at least nc / m chunks and an item
+        int lo = kCostChunk * (nc / m) + kCostItem, hi = M;  // cut_greedy(nc, hi) <= m throughout
+        if (lo > hi) lo = hi;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             if (cut_greedy(nc, mid, nullptr) <= m) hi = mid;
@@ -188,7 +192,13 @@ __global__ void __launch_bounds__(kPlanThreads) seg_plan_kernel(const ExtendPara
         const int b = b0 + lane;
         int ends[kMaxSegs];
         int m = 0;
-        if (b < B && req[b].nc >= 0) m = cut_request(req[b].nc, M, ends);
+        // the targets are compared on their greedy cuts (the equalised cut of the chosen one
+        // below costs no more)
+        if (b < B && req[b].nc >= 0) m = req[b].nc > 0 ? cut_greedy(req[b].nc, M, ends) : 0;
+        if (b < B && req[b].nc == 0) {
+            ends[0] = 0;
+            m = 1;
+        }
         int off = m;  // inclusive scan of the segment counts
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -225,13 +235,12 @@ __global__ void __launch_bounds__(kPlanThreads) seg_plan_kernel(const ExtendPara
         }
         __syncwarp();
         int worst = 0;
-        const long long items = (long long)R * H;
+        // at most 2P items (checked above): two rows of the deal; record of rank rk is rk / H
+        const int items = R * H;
         for (int j = lane; j < P; j += 32) {
-            int load = 0;
-            for (long long row = 0; row * P < items; ++row) {
-                const long long rk = row * P + ((row & 1) ? P - 1 - j : j);
-                if (rk < items) load += s_sorted[warp][rk / H];
-            }
+            int load = j < items ? s_sorted[warp][j / H] : 0;
+            const int rk = 2 * P - 1 - j;
+            if (rk < items) load += s_sorted[warp][rk / H];
             worst = max(worst, load);
         }
         span = __reduce_max_sync(0xffffffffu, worst);
@@ -567,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (base - raw);
-    pdl_wait();  // the plan is complete; the next kernel is let in at this CTA's end
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
     // Prologue chunks have a barrier pair per lambda-K lo buffer (stream index parity): kp_ready
     // (epilogue -> MMA: lambda K written) and pro_done (MMA -> epilogue: the chunk's MMAs done).
@@ -580,8 +588,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
     const int H = p.H;
-    const int nrec = hdr->nrec;
     auto no_finish = [](const SegItem &) {};
+
+    // Set-up touches only this CTA's shared and tensor memory, so it runs while the plan is
+    // still being made; everything after the wait sees the plan (and the previous kernel's
+    // writes).  The next kernel is let in at this CTA's end.
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
@@ -619,8 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
     const uint32_t tbase = bars->tmem_base;
     volatile int *abort_flag = &bars->abort_flag;
+    const int nrec = hdr->nrec;
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ TMA producer

@@ -158,6 +158,32 @@ def varlen_extend_many(seed: int = 0, B: int = 1024, lo: int = 32, hi: int = 512
     return w
 
 
+def varlen_extend_skewed(seed: int = 0, B: int = 8, n_long: int = 2, long_lo: int = 4096,
+                         long_hi: int = 8192, lo: int = 256, hi: int = 1024,
+                         num_slots: int = 64) -> Workload:
+    """Skewed varlen extend: 8 requests, the first two with lengths uniform in [4096, 8192] and the
+    other six in [256, 1024] (a couple of long prefills among short extends), H=16, layer 0 of
+    L=4; the even-indexed half carry prefix states; slots shuffled in a 64-slot pool.  The same
+    draw order as varlen_extend."""
+    g = torch.Generator().manual_seed(seed)
+    H, D = 16, HEAD_DIM
+    lens = torch.cat([torch.randint(long_lo, long_hi + 1, (n_long,), generator=g),
+                      torch.randint(lo, hi + 1, (B - n_long,), generator=g)])
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    T = int(cu[-1])
+    q, k, v = _qkv(g, T, H * D)
+    pm = torch.tensor([1 if b % 2 == 0 else 0 for b in range(B)], dtype=torch.uint8)
+    prefix = torch.zeros(B, H, D, D)
+    for b in range(B):
+        if pm[b]:
+            prefix[b] = torch.randn(H, D, D, generator=g) * 0.05
+    idx = torch.randperm(num_slots, generator=g)[:B].to(torch.int32)
+    return Workload(name=f"varlen_extend_skewed_b{B}_h16", kind="extend", H=H, D=D, layer_id=0,
+                    L=4, num_slots=num_slots, q=q, k=k, v=v, state_idx=idx, prefix_mask=pm,
+                    prefix_states=prefix, cu_seqlens=cu)
+
+
 def long_prefill(seed: int = 0, T: int = 32768, H: int = 32) -> Workload:
     """Long single-sequence prefill: one request of 32768 tokens, H=32, layer 5 of L=12, zero
     initial state; pool of 4 slots, the request in slot 1."""
@@ -322,4 +348,5 @@ WORKLOADS = {
     "varlen_extend_tracked": varlen_extend_tracked,
     "verify_commit": verify_commit,
     "varlen_extend_b1024": varlen_extend_many,
+    "varlen_extend_skewed": varlen_extend_skewed,
 }

@@ -7,8 +7,9 @@ Checked through the C ABI:
   * the plan the device leaves in the workspace: every request is covered once by contiguous
     segments that start on chunk boundaries, the last one flagged, the uneven batches really cut,
     at most two items per CTA, and the non-last segments dealt first;
-  * outputs and final states against the fp64 oracle, element by element: the varlen workload
-    (8 requests of 512-4096 tokens, 16 heads), a batch with empty, one-token and chunk-edge
+  * outputs and final states against the fp64 oracle, element by element: the skewed bench
+    workload, the varlen workload (8 requests of 512-4096 tokens, 16 heads, under a loose
+    max_seqlen), a batch with empty, one-token and chunk-edge
     requests, and a nearly flat decay that carries thousands of tokens through the prologues;
   * tracking snapshots inside the first segment, exactly at a segment start, inside the last
     segment and at the request's end, written into a head-major output;
@@ -237,3 +238,20 @@ def test_faulty_requests_in_a_balanced_batch():
     assert_close(to64(out)[rows], o_ref[rows], "balanced with faults: out")
     slots = [int(w.state_idx[b]) for b in ok]
     assert_close(pool.cpu().double().numpy()[slots], p_ref[slots], "balanced with faults: states")
+
+
+def test_skewed_workload_against_the_oracle():
+    """The bench's skewed workload (two requests of 4096-8192 tokens among six of 256-1024, 16
+    heads) at full size: it takes the balanced schedule by its own max_seqlen, cuts the long
+    requests, and matches the oracle element by element."""
+    w = workloads.varlen_extend_skewed()
+    lens = _lens(w)
+    assert max(lens) * w.B >= 2 * w.T and w.B * w.H <= _sms()
+    pool0 = w.materialize_pool()
+    out, pool, ws = _run(w)
+    la.poll_error()
+    recs = _plan(ws)
+    assert _check_plan(w, recs, _sms()) >= 2, "both long requests should be cut"
+    o_ref, p_ref = _oracle(w, pool0)
+    assert_close(to64(out), o_ref, "skewed workload: out")
+    _check_states(w, pool, pool0, p_ref, what="skewed workload")
