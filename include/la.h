@@ -202,7 +202,8 @@ la_status la_extend_workspace_size(int B, int T, int H, int D, int max_seqlen, s
  *   - A batch whose split plan needs more than 16 MiB of scratch is rejected with
  *     LA_ERR_UNSUPPORTED before anything is launched.  The largest plan is 1.5 x (SM count)
  *     matrices of 64 KiB -- 14.25 MiB on a 152-SM GB300 -- so every plan fits on devices of up to
- *     170 SMs; use la_extend with a workspace otherwise.
+ *     170 SMs; use la_extend with a workspace otherwise.  (The balanced schedule's plan, for
+ *     skewed one-wave batches, takes about 13 KiB.)
  *   - The first call on a device looks up the array's device address and caches it; make that
  *     first call before any stream capture.  Do not use it again in a process after
  *     cudaDeviceReset (the cached address belongs to the old context).

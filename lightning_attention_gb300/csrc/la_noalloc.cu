@@ -1,8 +1,9 @@
 // la_noalloc.cu -- la_extend_noalloc: the extend entry point for callers that cannot allocate
 // device memory.
 //
-// la_extend splits long requests of small batches into segments and needs scratch memory for it,
-// which the caller passes in (la_extend_workspace_size says how much).  Some callers have no way to
+// la_extend splits long requests of small batches into segments, plans skewed batches on the
+// device and keeps request records for large ones, and needs scratch memory for it, which the
+// caller passes in (la_extend_workspace_size says how much).  Some callers have no way to
 // obtain that buffer at the point where they run the extend step: a plugin inside a host framework
 // that owns the device's whole memory budget and hands the plugin nothing but its input and output
 // tensors, or a latency-critical loop in which cudaMalloc (with the implicit synchronisation it can
@@ -21,7 +22,8 @@
 //     loaded anew, so do not call this entry point again in that process.
 //   * Every call on a device shares the one array, and it keeps the last call's contents.  Nothing
 //     in it has to start at zero: each call writes every value it later reads (the initial-state
-//     copy and the block states) before reading it.  Calls that overlap on the GPU (for example on
+//     copy and the block states, the records, the balanced plan and its read counters) before
+//     reading it.  Calls that overlap on the GPU (for example on
 //     two streams at once) race on the array and give wrong results; serialise them.
 //   * The entry point calls no cudaMalloc, cudaFree or other allocating routine.
 #include <mutex>
