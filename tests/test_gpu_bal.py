@@ -255,3 +255,107 @@ def test_skewed_workload_against_the_oracle():
     o_ref, p_ref = _oracle(w, pool0)
     assert_close(to64(out), o_ref, "skewed workload: out")
     _check_states(w, pool, pool0, p_ref, what="skewed workload")
+
+
+def _draw_skewed(seed):
+    """A random skewed one-wave batch: 5-9 requests, 12 or 16 heads (so that B H fills more than
+    half of 152 SMs and no sequence split is planned), one or two of 1500-5000 tokens, the rest 0-700
+    with chunk edges; caller slopes log-uniform over six decades (some exactly zero)."""
+    rng = np.random.default_rng(5000 + seed)
+    B = int(rng.integers(5, 10))
+    H = int(rng.choice([12, 16])) if B >= 7 else 16  # B H > 76: more than half the SMs
+    edges = [0, 1, 127, 128, 129, 255, 256, 511]
+    lengths = [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(0, 700))
+               for _ in range(B)]
+    for i in rng.choice(B, size=int(rng.integers(1, 3)), replace=False):
+        lengths[int(i)] = int(rng.integers(1500, 5001))
+    top = int(np.argmax(lengths))
+    while lengths[top] * B < 2 * sum(lengths):  # skewed: the longest at least twice the mean
+        lengths[top] += 512
+    slopes = np.where(rng.random(H) < 0.15, 0.0, 10.0 ** rng.uniform(-6, np.log10(3), H))
+    prefix = [int(x) for x in rng.integers(0, 2, B)]
+    return rng, lengths, H, slopes.astype(np.float32), prefix
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_balanced_fuzz(seed):
+    """Random skewed batches with tracking snapshots at random offsets and the three output
+    layouts, against the oracle, with a valid plan."""
+    rng, lengths, H, slopes, prefix = _draw_skewed(seed)
+    B = len(lengths)
+    w = workloads.custom_extend(lengths, H=H, prefix=prefix, num_slots=2 * B + 2, seed=seed)
+    T = w.T
+    assert max(lengths) * B >= 2 * T and B * H <= _sms()
+    tl = np.array([int(rng.integers(0, n + 1)) if rng.random() < 0.7 else -1 for n in lengths],
+                  dtype=np.int32)
+    used = set(int(x) for x in w.state_idx.numpy())
+    free = [s for s in range(w.num_slots) if s not in used]
+    ti = np.array([free[b] if tl[b] >= 0 else -1 for b in range(B)], dtype=np.int32)
+    layout = ["packed", "per_head", "head_major"][seed % 3]
+    if layout == "head_major":
+        buf = torch.full((H, T, 128), 3.0, dtype=torch.bfloat16, device=DEV)
+        view = buf.transpose(0, 1)
+    elif layout == "per_head":
+        view = torch.full((T, H, 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    else:
+        view = torch.full((T, H * 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    pool0 = w.materialize_pool()
+    pool = pool0.to(DEV)
+    nbytes = la.extend_workspace_size(B, T, H, 128, max(lengths))
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=DEV)
+    la.extend(w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), torch.from_numpy(slopes).to(DEV), pool,
+              w.state_idx.to(DEV), w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV), out=view,
+              max_seqlen=max(lengths), workspace=ws, track_lens=torch.from_numpy(tl).to(DEV),
+              track_state_idx=torch.from_numpy(ti).to(DEV))
+    la.poll_error()
+    _check_plan(w, _plan(ws), _sms())
+    o_ref, p_ref = oracle.extend_tracked(w.q.float().numpy(), w.k.float().numpy(),
+                                         w.v.float().numpy(), slopes.astype(np.float64),
+                                         pool0.double().numpy(), w.state_idx.numpy(),
+                                         w.cu_seqlens.numpy(), w.prefix_mask.numpy(), tl, ti, H,
+                                         128)
+    tag = f"seed {seed} (B={B} H={H} lengths={lengths} {layout})"
+    assert_close(to64(view.reshape(T, H * 128)), o_ref, f"{tag}: out")
+    _check_states(w, pool, pool0, p_ref, extra=[int(x) for x in ti if x >= 0], what=tag)
+
+
+def test_balanced_graph_replay():
+    """The plan kernel and the balanced grid captured in a CUDA graph: two replays on new inputs
+    equal the eager calls bit for bit."""
+    lengths = [2600, 300, 400, 200, 700, 150]
+    w = workloads.custom_extend(lengths, H=16, prefix=[1, 0, 1, 0, 1, 1], seed=29, num_slots=16)
+    s = la.slopes(w.H, w.layer_id, w.L).to(DEV)
+    T, ms = w.T, max(lengths)
+    nbytes = la.extend_workspace_size(w.B, T, w.H, w.D, ms)
+    assert 0 < nbytes < 65536, "the batch must take the balanced schedule"
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    pool0 = w.materialize_pool()
+    qs, ks, vs = (torch.zeros(T, w.H * w.D, dtype=torch.bfloat16, device=DEV) for _ in range(3))
+    out = torch.empty(T, w.H * w.D, dtype=torch.bfloat16, device=DEV)
+    pool_g = pool0.to(DEV)
+    idx_d, cu_d, pm_d = w.state_idx.to(DEV), w.cu_seqlens.to(DEV), w.prefix_mask.to(DEV)
+    # warm-up outside the capture (module load, attributes)
+    la.extend(qs, ks, vs, s, pool0.to(DEV), idx_d, cu_d, pm_d, max_seqlen=ms, workspace=ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            la.extend(qs, ks, vs, s, pool_g, idx_d, cu_d, pm_d, out=out, max_seqlen=ms,
+                      workspace=ws)
+    la.poll_error()
+    for step in range(2):
+        gen = torch.Generator().manual_seed(700 + step)
+        q, k, v = (torch.randn(T, w.H * w.D, generator=gen).to(torch.bfloat16) for _ in range(3))
+        pool_g.copy_(pool0.to(DEV))
+        qs.copy_(q)
+        ks.copy_(k)
+        vs.copy_(v)
+        g.replay()
+        torch.cuda.synchronize()
+        pool_e = pool0.to(DEV)
+        o_e = la.extend(q.to(DEV), k.to(DEV), v.to(DEV), s, pool_e, idx_d, cu_d, pm_d,
+                        max_seqlen=ms, workspace=ws)
+        la.poll_error()
+        assert torch.equal(out.cpu(), o_e.cpu()), f"step {step}: replay != eager output"
+        assert torch.equal(pool_g.cpu().view(torch.int32), pool_e.cpu().view(torch.int32))
