@@ -114,7 +114,9 @@ __device__ __forceinline__ int seg_cost(int a, int e) {
 }
 
 // Sort key: non-last segments of cut requests first, then by decreasing cost.
-__device__ __forceinline__ int seg_key(int cost, bool nonlast) { return cost + (nonlast ? (1 << 24) : 0); }
+__device__ __forceinline__ int seg_key(int cost, bool nonlast) {
+    return cost + (nonlast ? (1 << 24) : 0);
+}
 
 // The request facts the plan needs, staged in shared memory by the validation step.
 struct PlanReq {
@@ -193,9 +195,11 @@ __global__ void __launch_bounds__(kPlanThreads) seg_plan_kernel(const ExtendPara
         int ends[kMaxSegs];
         int m = 0;
         // the targets are compared on their greedy cuts (the equalised cut of the chosen one
-        // below costs no more)
-        if (b < B && req[b].nc >= 0) m = req[b].nc > 0 ? cut_greedy(req[b].nc, M, ends) : 0;
-        if (b < B && req[b].nc == 0) {
+        // below costs no more); an empty request is one segment of no chunks
+        const int nc = b < B ? req[b].nc : -1;
+        if (nc > 0) {
+            m = cut_greedy(nc, M, ends);
+        } else if (nc == 0) {
             ends[0] = 0;
             m = 1;
         }
