@@ -215,3 +215,50 @@ def test_large_batch_longest_first_changes_only_the_schedule():
     assert_close(to64(out_a), o_ref, "large batch: out")
     idx = w.state_idx.numpy()
     assert_close(pool_a.cpu().double().numpy()[idx], p_ref[idx], "large batch: states")
+
+
+def test_batch_above_the_ranking_limit_runs_in_index_order():
+    """65,636 one-head requests (0-129 tokens, every other one with a prefix state) is above the
+    65,536 requests the longest-first ranking and the persistent grid's records take, so the
+    workspace asks for neither and one CTA per (request, head) runs in index order, about 430
+    waves.  Every 61st request (and the last one) is compared with the oracle run on those
+    requests alone; the slot past the batch keeps its bytes."""
+    B, H, D = 65536 + 100, 1, 128
+    cycle = [1, 2, 3, 0, 129, 5, 64, 7]
+    lengths = [cycle[b % len(cycle)] for b in range(B)]
+    cu = np.zeros(B + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lengths)
+    T = int(cu[-1])
+    assert la.extend_workspace_size(B, T, H, D, 129) == 0, "no ranking, no records, no split"
+    g = torch.Generator().manual_seed(23)
+    q, k, v = (torch.randn(T, H * D, generator=g).to(torch.bfloat16) for _ in range(3))
+    pm = torch.tensor([b % 2 for b in range(B)], dtype=torch.uint8)
+    # the prefix states as a pattern cheap to rebuild on both sides: slot b holds 0.05 * N(0,1)
+    # values drawn per slot from a small table, so that 4.3 GB never sits on the host
+    table = torch.randn(16, H, D, D, generator=g) * 0.05
+    pool = torch.empty(B + 1, H, D, D, device=DEV)
+    tdev = table.to(DEV)
+    for s0 in range(0, B + 1, 4096):
+        s1 = min(B + 1, s0 + 4096)
+        sl = torch.arange(s0, s1, device=DEV)
+        pool[s0:s1] = tdev[sl % 16]
+    sentinel = pool[B].clone()
+    idx = torch.arange(B, dtype=torch.int32)
+    s = la.slopes(H, 1, 3)
+    out = la.extend(q.to(DEV), k.to(DEV), v.to(DEV), s.to(DEV), pool, idx.to(DEV),
+                    torch.from_numpy(cu.astype(np.int32)).to(DEV), pm.to(DEV), max_seqlen=129)
+    la.poll_error()
+    assert torch.equal(pool[B].view(torch.int32), sentinel.view(torch.int32))
+    pick = sorted(set(range(0, B, 61)) | {B - 1})
+    sub_len = [lengths[b] for b in pick]
+    sub_cu = np.zeros(len(pick) + 1, dtype=np.int32)
+    sub_cu[1:] = np.cumsum(sub_len)
+    rows = torch.from_numpy(np.concatenate([np.arange(cu[b], cu[b + 1]) for b in pick]))
+    pool0 = np.stack([table[b % 16].double().numpy() for b in pick])
+    o_ref, p_ref = oracle.extend(q[rows].float().numpy(), k[rows].float().numpy(),
+                                 v[rows].float().numpy(), oracle_slopes_fp32(H, 1, 3), pool0,
+                                 np.arange(len(pick), dtype=np.int32), sub_cu,
+                                 pm.numpy()[pick], H, D)
+    assert_close(to64(out[rows.to(DEV)]), o_ref, "above the ranking limit: out")
+    got = pool[torch.tensor(pick, device=DEV)].cpu().double().numpy()
+    assert_close(got, p_ref, "above the ranking limit: states")
