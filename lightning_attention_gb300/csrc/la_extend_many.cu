@@ -128,22 +128,21 @@ __device__ __forceinline__ void seed_state(const ExtendParams &p, const Item &it
     if (r.nchunks > 0) tmem_st_wait();
 }
 
-// The final state of an item from TMEM (left unscaled by its last chunk) into its pool slot, and
-// into the tracking slot when the snapshot is at the request's end.
-template <bool kEx>
-__device__ __forceinline__ void final_state(const ExtendParams &p, const Item &it, uint32_t t_s,
-                                            int col_base, int i, bool snap) {
+// This thread's row of an item's final state from TMEM (left unscaled by its last chunk) into the
+// staging tiles for the TMA store: four boxes of [128 rows][32 fp32 columns], 16 KiB apart, each
+// row's eight 16-byte chunks placed with the 128-byte swizzle the state map uses.
+__device__ __forceinline__ void stage_final_state(uint32_t t_s, int col_base, int i, uint8_t *stg) {
 #pragma unroll 1
     for (int sub = 0; sub < 2; ++sub) {
         const int col0 = col_base + sub * 32;
         uint32_t w[32];
         tmem_ld32(t_s + (uint32_t)col0, w);
         tmem_ld_wait_regs(w);
-        float S[32];
+        uint8_t *row = stg + (col0 >> 5) * 16384 + i * 128;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) S[x] = __uint_as_float(w[x]);
-        store_state_row(p.pool, it.r.slot, p.H, it.h, i, col0, S);
-        if (kEx && snap) store_state_row(p.pool, it.r.tslot, p.H, it.h, i, col0, S);
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(row + ((c ^ (i & 7)) << 4)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
     }
 }
 
@@ -152,13 +151,19 @@ template <bool kEx>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_many_kernel(const __grid_constant__ CUtensorMap tq,
                        const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const ExtendParams p) {
+                       const __grid_constant__ CUtensorMap tv,
+                       const __grid_constant__ CUtensorMap tsm, const ExtendParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (base - raw);
     pdl_wait();  // the next kernel is let in at this CTA's end
     Bars *bars = reinterpret_cast<Bars *>(sm + OFF_BAR);
+    // The hand-over of a finished item's state: stg_ready (the epilogue warps have staged their
+    // rows of it in the S_hi / S_lo tiles) and stg_free (the TMA stores have read the tiles, which
+    // the next item's start may overwrite).
+    uint64_t *stg_ready = reinterpret_cast<uint64_t *>(sm + OFF_BAR + sizeof(Bars));
+    uint64_t *stg_free = stg_ready + 1;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
@@ -181,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->u_full, 1);
         mbar_init(&bars->o_full, 1);
         mbar_init(&bars->drain, 1);
+        mbar_init(stg_ready, kEpiWarps);
+        mbar_init(stg_free, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -192,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&tsm);
     }
     tc_fence_before();
     __syncthreads();
@@ -264,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         bool ok = true;
         int gc = 0;
+        int nhand = 0;  // hand-overs so far (the staging barriers' phases)
         while (have && ok) {
             // the item's factors, as in the one-CTA-per-item kernel
             const float slope = p.slopes[cur.h];
@@ -318,8 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        p.pool, r_cur.tslot, p.H, h_cur, 0);
                 } else {
                     // MMA4 and (by issue order) MMA2 of the item's last chunk are done: its final
-                    // state leaves TMEM, and the next item's S0 takes the operand tiles and TMEM
-                    final_state<kEx>(p, cur, t_s, col_base, i, kEx && cs + r == r_cur.sp);
+                    // state leaves TMEM through the S_hi / S_lo tiles (free now) and TMA stores,
+                    // and the next item's S0 takes the operand tiles and TMEM once the stores have
+                    // read them.  Staged this way the epilogue waits for a shared-memory read
+                    // instead of 64 KiB of global stores.
+                    stage_final_state(t_s, col_base, i, s_hi);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(stg_ready);
+                    if (threadIdx.x == 0) {
+                        if (wait_bar(stg_ready, nhand & 1, limit, abort_flag, p.err)) {
+                            const int y = (cur.r.slot * p.H + cur.h) * kHeadDim;
+#pragma unroll
+                            for (int bx = 0; bx < 4; ++bx)
+                                tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, y);
+                            if (kEx && cs + r == r_cur.sp) {  // the snapshot at the request's end
+                                const int ys = (cur.r.tslot * p.H + cur.h) * kHeadDim;
+#pragma unroll
+                                for (int bx = 0; bx < 4; ++bx)
+                                    tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, ys);
+                            }
+                            bulk_commit_group();
+                            bulk_wait_group_read0();
+                        }
+                        mbar_arrive(stg_free);
+                    }
+                    if (!(ok = warp_wait_bar(stg_free, nhand & 1, limit, abort_flag, p.err))) break;
+                    ++nhand;
                     Item nx;
                     have_nx = walk.take(p, nx, finish);
                     if (have_nx) {
@@ -344,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // the final-state stores this thread issued are complete before the CTA ends
+    if (threadIdx.x == 0) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -352,6 +388,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tmem_dealloc(tbase, kTmemCols);
     }
+}
+
+static_assert(sizeof(Bars) + 2 * sizeof(uint64_t) <= SZ_BAR, "barrier block with the staging pair");
+static_assert(OFF_SLO == OFF_SHI + SZ_T && SZ_T == 2 * 16384 && OFF_SHI % 1024 == 0,
+              "the final state's staging: four 16 KiB boxes over S_hi and S_lo, swizzle-aligned");
+
+// The state pool as a TMA map: rows of 128 fp32 (row (slot H + h) 128 + i of slot, head h), boxes
+// of 32 columns x 128 rows (a quarter of one state) with the 128-byte swizzle.
+typedef CUresult (*EncodeTiledFnM)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_state_map(CUtensorMap *m, float *pool, long long rows) {
+    static EncodeTiledFnM fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFnM>(f);
+    });
+    if (!fn || rows <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * sizeof(float)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kHeadDim};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Item records: one thread per request computes its rank (request_rank) and writes its geometry
@@ -405,15 +473,18 @@ cudaError_t launch_extend_many(const ExtendParams &p, ItemRec *recs, int ctas,
     cudaError_t e = launch_pdl(item_records_kernel, dim3((unsigned)((p.B + 255) / 256)), dim3(256),
                                0, stream, p, recs);
     if (e != cudaSuccess) return e;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tsm;
     memset(&tq, 0, sizeof(tq));
     memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv));
+    memset(&tsm, 0, sizeof(tsm));
     if (p.T > 0) {
         if (!make_token_map_full(&tq, p.q, p.T, p.H) || !make_token_map_full(&tk, p.k, p.T, p.H) ||
             !make_token_map_full(&tv, p.v, p.T, p.H))
             return cudaErrorInvalidValue;
     }
+    if (!make_state_map(&tsm, p.pool, (long long)p.num_slots * p.H * kHeadDim))
+        return cudaErrorInvalidValue;
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -436,9 +507,9 @@ cudaError_t launch_extend_many(const ExtendParams &p, ItemRec *recs, int ctas,
     pw.recs = recs;
     if (p.track_lens != nullptr || p.out_rs != (long long)p.H * kHeadDim || p.out_hs != kHeadDim)
         return launch_pdl(extend_many_kernel<true>, dim3((unsigned)ctas), dim3(kThreads),
-                          kSmemBytes, stream, tq, tk, tv, pw);
+                          kSmemBytes, stream, tq, tk, tv, tsm, pw);
     return launch_pdl(extend_many_kernel<false>, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes,
-                      stream, tq, tk, tv, pw);
+                      stream, tq, tk, tv, tsm, pw);
 }
 
 }  // namespace la
