@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kEx) cs_next = cs + r;
                 const bool last = c + 1 == r_cur.nchunks;
                 // the next item's initial state rows into L2 a chunk ahead (its record is in)
+                // the next item's initial state rows into L2 a chunk ahead (its record is in)
                 if (last && walk.more && walk.nxt.valid() && walk.nxt.prefix()) {
                     const float *nrow = p.pool + (((size_t)walk.nxt.r.slot * p.H + walk.nxt.h) *
                                                       kHeadDim + i) * kHeadDim + (size_t)col_base;
@@ -327,39 +328,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        p.pool, r_cur.tslot, p.H, h_cur, 0);
                 } else {
                     // MMA4 and (by issue order) MMA2 of the item's last chunk are done: its final
-                    // state leaves TMEM through the S_hi / S_lo tiles (free now) and TMA stores,
-                    // and the next item's S0 takes the operand tiles and TMEM once the stores have
-                    // read them.  Staged this way the epilogue waits for a shared-memory read
-                    // instead of 64 KiB of global stores.
+                    // state leaves TMEM through the S_hi / S_lo tiles (free now) and TMA stores.
+                    // While the stores read the tiles the epilogue runs the chunk's output pass
+                    // (which does not touch them); then the next item's S0 takes the operand tiles
+                    // and TMEM.  This keeps 64 KiB of global stores off the chain between the two
+                    // items.
                     stage_final_state(t_s, col_base, i, s_hi);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(stg_ready);
-                    if (threadIdx.x == 0) {
-                        if (wait_bar(stg_ready, nhand & 1, limit, abort_flag, p.err)) {
-                            const int y = (cur.r.slot * p.H + cur.h) * kHeadDim;
+                    if (threadIdx.x == 0 && wait_bar(stg_ready, nhand & 1, limit, abort_flag, p.err)) {
+                        const int y = (cur.r.slot * p.H + cur.h) * kHeadDim;
+#pragma unroll
+                        for (int bx = 0; bx < 4; ++bx)
+                            tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, y);
+                        if (kEx && cs + r == r_cur.sp) {  // the snapshot at the request's end
+                            const int ys = (cur.r.tslot * p.H + cur.h) * kHeadDim;
 #pragma unroll
                             for (int bx = 0; bx < 4; ++bx)
-                                tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, y);
-                            if (kEx && cs + r == r_cur.sp) {  // the snapshot at the request's end
-                                const int ys = (cur.r.tslot * p.H + cur.h) * kHeadDim;
-#pragma unroll
-                                for (int bx = 0; bx < 4; ++bx)
-                                    tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, ys);
-                            }
-                            bulk_commit_group();
-                            bulk_wait_group_read0();
+                                tma_store_2d(&tsm, s_hi + bx * 16384, bx * 32, ys);
                         }
+                        bulk_commit_group();
+                    }
+                    if (!(ok = warp_wait_bar(&bars->o_full, gc & 1, limit, abort_flag, p.err))) {
+                        if (threadIdx.x == 0) mbar_arrive(stg_free);
+                        break;
+                    }
+                    tc_fence_after();
+                    out_pass<2>(tbase + lane_off, col_base, gam, lane, q, r, p.out, r_cur.t0 + cs,
+                                row_stride, (size_t)h_cur * head_stride);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->o_free);
+                    Item nx;
+                    have_nx = walk.take(p, nx, finish);
+                    if (threadIdx.x == 0) {
+                        bulk_wait_group_read0();
                         mbar_arrive(stg_free);
                     }
                     if (!(ok = warp_wait_bar(stg_free, nhand & 1, limit, abort_flag, p.err))) break;
                     ++nhand;
-                    Item nx;
-                    have_nx = walk.take(p, nx, finish);
                     if (have_nx) {
                         seed_state<kEx>(p, nx, t_s, col_base, s_hi, s_lo, i);
                         cur = nx;
                     }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->s_ready);
+                    continue;  // the chunk's output pass is done
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
