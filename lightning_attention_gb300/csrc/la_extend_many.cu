@@ -128,6 +128,45 @@ __device__ __forceinline__ void seed_state(const ExtendParams &p, const Item &it
     if (r.nchunks > 0) tmem_st_wait();
 }
 
+// Where box bx (state columns 32 bx .. 32 bx + 31, fp32, 128-byte swizzled) of an S0 loaded
+// through the staging tiles lands: each box over the rows that will hold the same columns' bf16
+// hi or lo, so that a thread converting its row overwrites only values it has read itself.
+__device__ __forceinline__ uint32_t s0_box_offset(int bx) {
+    return (uint32_t)((bx & 1) * 32768 + (bx >> 1) * 16384);
+}
+
+// The start of item it (with chunks and a prefix) from its S0 in the staging tiles: this thread's
+// row i, columns col_base .. col_base + 63 (boxes 2 cw and 2 cw + 1), read whole before it is
+// overwritten by its bf16 pair for the first MMA2; e^{-s r0} S0 into TMEM for the first MMA4.
+__device__ __forceinline__ void seed_from_tiles(const ExtendParams &p, const Item &it,
+                                                uint32_t t_s, int col_base, uint8_t *s_hi,
+                                                uint8_t *s_lo, int i) {
+    float S[64];
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+        const uint8_t *row = s_hi + s0_box_offset((col_base >> 5) + sub) + i * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 f = *reinterpret_cast<const float4 *>(row + ((c ^ (i & 7)) << 4));
+            S[sub * 32 + 4 * c] = f.x;
+            S[sub * 32 + 4 * c + 1] = f.y;
+            S[sub * 32 + 4 * c + 2] = f.z;
+            S[sub * 32 + 4 * c + 3] = f.w;
+        }
+    }
+    const float d0s = expf(-p.slopes[it.h] * (float)chunk_len(false, 0, it.r.sp, it.r.n));
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+        const int col0 = col_base + sub * 32;
+        store_state_split(s_hi, s_lo, i, col0 >> 6, (col0 >> 5) & 1, S + sub * 32);
+        uint32_t w[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(S[sub * 32 + x] * d0s);
+        tmem_st32(t_s + (uint32_t)col0, w);
+    }
+    tmem_st_wait();
+}
+
 // This thread's row of an item's final state from TMEM (left unscaled by its last chunk) into the
 // staging tiles for the TMA store: four boxes of [128 rows][32 fp32 columns], 16 KiB apart, each
 // row's eight 16-byte chunks placed with the 128-byte swizzle the state map uses.
@@ -164,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the next item's start may overwrite).
     uint64_t *stg_ready = reinterpret_cast<uint64_t *>(sm + OFF_BAR + sizeof(Bars));
     uint64_t *stg_free = stg_ready + 1;
+    // s0_full: the next item's S0 has landed in the staging tiles (a TMA load, plain variant)
+    uint64_t *s0_full = stg_ready + 2;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
@@ -188,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->drain, 1);
         mbar_init(stg_ready, kEpiWarps);
         mbar_init(stg_free, 1);
+        mbar_init(s0_full, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -273,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int gc = 0;
         int nhand = 0;  // hand-overs so far (the staging barriers' phases)
+        int nload = 0;  // S0 loads through the staging tiles so far (s0_full's phases)
+        int s0_issued = 0;  // of them issued (thread 0): an abort may leave one unwaited
         while (have && ok) {
             // the item's factors, as in the one-CTA-per-item kernel
             const float slope = p.slopes[cur.h];
@@ -362,13 +406,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&bars->o_free);
                     Item nx;
                     have_nx = walk.take(p, nx, finish);
+                    // a prefix S0 comes in by one TMA load into the tiles, once the stores have
+                    // read them (plain variant; the options variant loads it per thread)
+                    const bool tma_s0 = !kEx && have_nx && nx.prefix();
                     if (threadIdx.x == 0) {
                         bulk_wait_group_read0();
+                        if (tma_s0) {
+                            const int y = (nx.r.slot * p.H + nx.h) * kHeadDim;
+                            mbar_arrive_expect_tx(s0_full, 4 * 16384);
+#pragma unroll
+                            for (int bx = 0; bx < 4; ++bx)
+                                tma_load_2d(s_hi + s0_box_offset(bx), &tsm, s0_full, bx * 32, y);
+                            ++s0_issued;
+                        }
                         mbar_arrive(stg_free);
                     }
                     if (!(ok = warp_wait_bar(stg_free, nhand & 1, limit, abort_flag, p.err))) break;
                     ++nhand;
-                    if (have_nx) {
+                    if (tma_s0) {
+                        if (!(ok = warp_wait_bar(s0_full, nload & 1, limit, abort_flag, p.err)))
+                            break;
+                        ++nload;
+                        seed_from_tiles(p, nx, t_s, col_base, s_hi, s_lo, i);
+                        cur = nx;
+                    } else if (have_nx) {
                         seed_state<kEx>(p, nx, t_s, col_base, s_hi, s_lo, i);
                         cur = nx;
                     }
@@ -393,6 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             have = have_nx;
         }
+        // an S0 load issued and not waited for (the loop left on an abort) lands before the
+        // shared memory goes away
+        if (threadIdx.x == 0 && s0_issued > nload) {
+            int dummy = 0;
+            wait_bar(s0_full, (s0_issued - 1) & 1, kDrainLimitNs, &dummy, p.err);
+        }
     }
 
     // the final-state stores this thread issued are complete before the CTA ends
@@ -407,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-static_assert(sizeof(Bars) + 2 * sizeof(uint64_t) <= SZ_BAR, "barrier block with the staging pair");
+static_assert(sizeof(Bars) + 3 * sizeof(uint64_t) <= SZ_BAR, "barrier block with the staging barriers");
 static_assert(OFF_SLO == OFF_SHI + SZ_T && SZ_T == 2 * 16384 && OFF_SHI % 1024 == 0,
               "the final state's staging: four 16 KiB boxes over S_hi and S_lo, swizzle-aligned");
 
