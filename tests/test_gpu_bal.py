@@ -359,3 +359,21 @@ def test_balanced_graph_replay():
         la.poll_error()
         assert torch.equal(out.cpu(), o_e.cpu()), f"step {step}: replay != eager output"
         assert torch.equal(pool_g.cpu().view(torch.int32), pool_e.cpu().view(torch.int32))
+
+
+def test_many_requests_one_head():
+    """150 one-head requests (one of 6000 tokens among short ones): the planner walks the
+    requests 32 at a time in every warp, and records stay within the limits."""
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(0, 300, size=150)]
+    lens[77] = 6000
+    w = workloads.custom_extend(lens, H=1, prefix=[b % 3 == 0 for b in range(150)], seed=33,
+                                num_slots=160)
+    assert max(lens) * w.B >= 2 * w.T and w.B * w.H <= _sms()
+    pool0 = w.materialize_pool()
+    out, pool, ws = _run(w)
+    la.poll_error()
+    assert _check_plan(w, _plan(ws), _sms()) >= 1
+    o_ref, p_ref = _oracle(w, pool0)
+    assert_close(to64(out), o_ref, "150 requests, one head: out")
+    _check_states(w, pool, pool0, p_ref, what="150 requests, one head")
